@@ -1,0 +1,215 @@
+"""Seeded synthetic inputs for sparse MLA attention (prefill and decode).
+
+The only module that both the CUDA path's tests/benchmark and the CPU oracle
+consume.  It draws random numbers and packs them into the cache row format; it
+holds none of the attention arithmetic (no dequantisation, no softmax).
+
+Row format written here (FlashInfer PR #4802 "Refactor Sparse MLA SM120",
+review note on the DSv3.2 per-token KV layout): bytes ``[0:512)`` e4m3 codes,
+``[512:528)`` four little-endian fp32 scales (one per 128 codes, powers of
+two), ``[528:656)`` 64 bf16 rope values.
+
+Recipe: nope values ``x ~ N(0,1)``; per 128-block ``scale =
+2^ceil(log2(amax/448))``; stored code = e4m3(x / scale) rounded to nearest
+even (torch's float8_e4m3fn cast); rope ``~ N(0,1)`` rounded to bf16; q ``~
+N(0,1)`` rounded to bf16; sinks ``N(0,1)`` (or zeros); unique random indices
+per query row.  numpy PCG64, seed 0 unless stated.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+ROW_BYTES = 656
+PAGE = 64
+D_QK = 576
+D_V = 512
+POISON = 0x7FFFFFFF
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    q: torch.Tensor  # bf16 [T, H, 576] (CPU)
+    kv: torch.Tensor  # uint8 [num_pages, 64, 656] (CPU)
+    indices: torch.Tensor  # int32 [T, ld], ld >= topk (CPU)
+    topk: int
+    sm_scale: float
+    topk_length: Optional[torch.Tensor] = None  # int32 [T]
+    attn_sink: Optional[torch.Tensor] = None  # fp32 [H]
+    block_table: Optional[torch.Tensor] = None  # int32 [B, max_pages]
+    tokens_per_req: int = 1
+    decode: bool = False
+    meta: dict = dataclasses.field(default_factory=dict)
+
+    @property
+    def T(self):
+        return self.q.shape[0]
+
+    @property
+    def H(self):
+        return self.q.shape[1]
+
+    @property
+    def num_pages(self):
+        return self.kv.shape[0]
+
+
+def pow2_scale_exponent(amax: np.ndarray) -> np.ndarray:
+    """Exponent e with 2^e = 2^ceil(log2(amax/448)), computed exactly via frexp."""
+    v = np.asarray(amax, dtype=np.float64) / 448.0
+    m, e = np.frexp(np.where(v > 0, v, 1.0))
+    e = e - (m == 0.5).astype(e.dtype)
+    return np.where(v > 0, e, 0)
+
+
+def make_cache(rng: np.random.Generator, num_pages: int, chunk_rows: int = 65536) -> torch.Tensor:
+    """A paged cache ``[num_pages, 64, 656]`` of uint8 rows (see module docstring)."""
+    n_rows = num_pages * PAGE
+    out = np.empty((n_rows, ROW_BYTES), dtype=np.uint8)
+    for lo in range(0, n_rows, chunk_rows):
+        hi = min(n_rows, lo + chunk_rows)
+        n = hi - lo
+        x = rng.standard_normal((n, 512), dtype=np.float32)
+        amax = np.abs(x.reshape(n, 4, 128)).max(axis=2)
+        e = pow2_scale_exponent(amax)
+        scale = np.ldexp(np.float32(1.0), e).astype(np.float32)  # [n, 4]
+        y = (x.reshape(n, 4, 128) / scale[:, :, None]).reshape(n, 512)
+        y = np.clip(y, -448.0, 448.0)
+        codes = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        rope = rng.standard_normal((n, 64), dtype=np.float32)
+        rope_bits = torch.from_numpy(rope).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint8)
+        out[lo:hi, 0:512] = codes
+        out[lo:hi, 512:528] = scale.astype("<f4").view(np.uint8).reshape(n, 16)
+        out[lo:hi, 528:656] = rope_bits.reshape(n, 128)
+    return torch.from_numpy(out.reshape(num_pages, PAGE, ROW_BYTES))
+
+
+def unique_rows(rng: np.random.Generator, T: int, K: int, N: int) -> np.ndarray:
+    """``T`` rows of ``K`` distinct integers drawn uniformly from ``[0, N)``."""
+    assert K <= N
+    if 2 * K > N:
+        keys = rng.random((T, N))
+        return np.argsort(keys, axis=1)[:, :K].astype(np.int64)
+    out = rng.integers(0, N, size=(T, K), dtype=np.int64)
+    for _ in range(1000):
+        order = np.argsort(out, axis=1, kind="stable")
+        srt = np.take_along_axis(out, order, axis=1)
+        d = np.zeros_like(srt, dtype=bool)
+        d[:, 1:] = srt[:, 1:] == srt[:, :-1]
+        if not d.any():
+            return out
+        dup = np.zeros_like(d)
+        np.put_along_axis(dup, order, d, axis=1)
+        out[dup] = rng.integers(0, N, size=int(dup.sum()), dtype=np.int64)
+    raise RuntimeError("unique_rows did not converge")
+
+
+def _bf16(rng, shape):
+    return torch.from_numpy(rng.standard_normal(shape, dtype=np.float32)).to(torch.bfloat16)
+
+
+def make_prefill(name, T, H, ctx, topk, seed=0, sink="normal", ld=None, ragged=False,
+                 neg_prob=0.0, sm_scale=None) -> Workload:
+    """Flat-addressed prefill: one context of ``ctx`` rows, ``topk`` unique ids per row.
+
+    ``ragged``: topk_length ~ U{1..topk} per row and entries past it set to -1.
+    ``ld``: index row stride (columns ``topk..ld`` hold a poison value).
+    ``neg_prob``: each entry independently replaced by -1 with this probability.
+    """
+    rng = np.random.default_rng(seed)
+    assert ctx % PAGE == 0
+    kv = make_cache(rng, ctx // PAGE)
+    q = _bf16(rng, (T, H, D_QK))
+    ld = topk if ld is None else ld
+    idx = np.full((T, ld), POISON, dtype=np.int64)
+    idx[:, :topk] = unique_rows(rng, T, topk, ctx)
+    tl = None
+    if ragged:
+        lens = rng.integers(1, topk + 1, size=T)
+        tl = torch.from_numpy(lens.astype(np.int32))
+        cols = np.arange(topk)[None, :]
+        idx[:, :topk] = np.where(cols < lens[:, None], idx[:, :topk], -1)
+    if neg_prob > 0:
+        drop = rng.random((T, topk)) < neg_prob
+        idx[:, :topk] = np.where(drop, -1, idx[:, :topk])
+    if sink == "normal":
+        s = torch.from_numpy(rng.standard_normal(H).astype(np.float32))
+    elif sink == "zeros":
+        s = torch.zeros(H, dtype=torch.float32)
+    else:
+        s = None
+    return Workload(
+        name=name, q=q, kv=kv, indices=torch.from_numpy(idx.astype(np.int32)), topk=topk,
+        sm_scale=(1.0 / math.sqrt(D_QK)) if sm_scale is None else sm_scale,
+        topk_length=tl, attn_sink=s,
+        meta=dict(T=T, H=H, ctx=ctx, topk=topk, ld=ld, seed=seed, ragged=ragged,
+                  neg_prob=neg_prob, sink=sink))
+
+
+def make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=0, sink="normal") -> Workload:
+    """Paged decode: ``n_req`` requests, each its own context of ``ctx_per_req``
+    logical positions mapped through a block table that is one shuffled
+    permutation of all pages; ``topk`` unique logical ids per query token."""
+    rng = np.random.default_rng(seed)
+    assert ctx_per_req % PAGE == 0
+    pages_per_req = ctx_per_req // PAGE
+    num_pages = n_req * pages_per_req
+    kv = make_cache(rng, num_pages)
+    T = n_req * tokens_per_req
+    q = _bf16(rng, (T, H, D_QK))
+    bt = rng.permutation(num_pages).reshape(n_req, pages_per_req)
+    idx = unique_rows(rng, T, topk, ctx_per_req)
+    if sink == "normal":
+        s = torch.from_numpy(rng.standard_normal(H).astype(np.float32))
+    elif sink == "zeros":
+        s = torch.zeros(H, dtype=torch.float32)
+    else:
+        s = None
+    return Workload(
+        name=name, q=q, kv=kv, indices=torch.from_numpy(idx.astype(np.int32)), topk=topk,
+        sm_scale=1.0 / math.sqrt(D_QK), attn_sink=s,
+        block_table=torch.from_numpy(bt.astype(np.int32)), tokens_per_req=tokens_per_req,
+        decode=True,
+        meta=dict(n_req=n_req, tokens_per_req=tokens_per_req, H=H, ctx_per_req=ctx_per_req,
+                  topk=topk, seed=seed, sink=sink))
+
+
+# The five workloads, named by what they are.
+def tiny_prefill(seed=0):
+    return make_prefill("tiny_prefill_T4_H8_ctx256_k64", T=4, H=8, ctx=256, topk=64,
+                        seed=seed, sink="zeros")
+
+
+def prefill_16k(topk=512, seed=0, T=1024):
+    return make_prefill(f"prefill_T{T}_H64_ctx16384_k{topk}", T=T, H=64, ctx=16384,
+                        topk=topk, seed=seed)
+
+
+def fewhead_prefill(seed=0, T=8192):
+    return make_prefill(f"fewhead_prefill_T{T}_H8_ctx32768_k640_ld1024_ragged", T=T, H=8,
+                        ctx=32768, topk=640, seed=seed, ld=1024, ragged=True)
+
+
+def batched_decode(seed=0, n_req=64):
+    return make_decode(f"decode_{n_req}req_x2_H64_ctx32768_k2048_paged", n_req=n_req,
+                       tokens_per_req=2, H=64, ctx_per_req=32768, topk=2048, seed=seed)
+
+
+def large_prefill(seed=0, T=4096):
+    return make_prefill(f"large_prefill_T{T}_H128_ctx131072_k2048_neg0.1", T=T, H=128,
+                        ctx=131072, topk=2048, seed=seed, neg_prob=0.1)
+
+
+WORKLOADS = {
+    "tiny": tiny_prefill,
+    "prefill16k_k512": lambda seed=0: prefill_16k(512, seed),
+    "prefill16k_k1024": lambda seed=0: prefill_16k(1024, seed),
+    "fewhead": fewhead_prefill,
+    "decode": batched_decode,
+    "large": large_prefill,
+}

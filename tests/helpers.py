@@ -1,0 +1,59 @@
+"""Shared test helpers: device transfer, oracle calls on sampled tokens, tolerances."""
+import numpy as np
+import torch
+
+import oracle.sparse_mla_oracle as O
+
+# Tolerances on out (bf16) and lse (fp32) against the fp64 oracle.
+OUT_MAX_ABS = 2e-2
+OUT_MEAN_ABS = 2e-3
+LSE_ABS = 1e-3
+
+
+def to_dev(wl, device="cuda"):
+    d = {}
+    for k in ("q", "kv", "indices", "topk_length", "attn_sink", "block_table"):
+        v = getattr(wl, k)
+        d[k] = None if v is None else v.to(device)
+    return d
+
+
+def oracle_for(wl, tokens=None, indices=None, topk=None, topk_length="wl", attn_sink="wl"):
+    q = wl.q.to(torch.float64).numpy() if tokens is None else wl.q[torch.as_tensor(tokens)].to(torch.float64).numpy()
+    idx = (wl.indices if indices is None else indices).numpy()
+    tl = wl.topk_length if topk_length == "wl" else topk_length
+    sk = wl.attn_sink if attn_sink == "wl" else attn_sink
+    bt = None if wl.block_table is None else wl.block_table.numpy()
+    sel = None if tokens is None else np.asarray(tokens)
+    if sel is not None:
+        # q was already sliced; pass positions so indices/lengths/requests line up
+        full_q = np.zeros((wl.T, wl.H, 576))
+        full_q[sel] = q
+        q = full_q
+    return O.sparse_mla_forward(q, wl.kv.numpy(), idx, topk or wl.topk, wl.sm_scale,
+                                topk_length=None if tl is None else tl.numpy(),
+                                attn_sink=None if sk is None else sk.numpy().astype(np.float64),
+                                block_table=bt, tokens_per_req=wl.tokens_per_req, tokens=sel)
+
+
+def assert_close(out_gpu, lse_gpu, out_ref, lse_ref, tag=""):
+    o = out_gpu.float().cpu().numpy().astype(np.float64)
+    l = lse_gpu.float().cpu().numpy().astype(np.float64)
+    assert o.shape == out_ref.shape, (o.shape, out_ref.shape)
+    assert np.isfinite(o).all(), f"{tag}: non-finite outputs"
+    err = np.abs(o - out_ref)
+    assert err.max() <= OUT_MAX_ABS, f"{tag}: out max_abs {err.max():.3e}"
+    assert err.mean() <= OUT_MEAN_ABS, f"{tag}: out mean_abs {err.mean():.3e}"
+    ninf_g, ninf_r = np.isneginf(l), np.isneginf(lse_ref)
+    assert np.array_equal(ninf_g, ninf_r), f"{tag}: -inf LSE pattern differs"
+    if (~ninf_r).any():
+        le = np.abs(l[~ninf_r] - lse_ref[~ninf_r])
+        assert le.max() <= LSE_ABS, f"{tag}: lse max_abs {le.max():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def sample_tokens(T, n, seed=0, must=()):
+    rng = np.random.default_rng(seed)
+    pick = set(int(x) for x in must if 0 <= x < T)
+    pick.update(int(x) for x in rng.choice(T, size=min(n, T), replace=False))
+    return np.array(sorted(pick))
