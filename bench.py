@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse MLA forward on GB300 (one JSON line on rank 0).
+
+Default workload: prefill at the 16k footprint -- T=1024 query tokens, H=64,
+context 16384 (256 pages of 64 rows, 656-byte FP8 rows), topk 512 then 1024
+unique indices per query row, per-head sinks, bf16 q.  One step runs the
+whole hot path over that batch at both widths (two prefill launches).
+``--workload`` selects the other workloads (few-head, decode, large) for
+profiling; their numbers go to the same JSON format.
+
+value: query tokens processed per second (each width counts its 1024 tokens),
+device-timed with CUDA events around the launches, inputs resident in HBM,
+L2 flushed (256 MiB write) between steps.  e2e: the same through the public
+API from pinned host buffers with the H2D copy of q/indices and the D2H copy
+of out/lse inside the timed region.  cpu_baseline / --impl reference: the
+CPU oracle on a bounded sample of tokens on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA query-tokens/s at 1 GB300; % of roofline (tensor-core or HBM)"
+UNIT = "query-tokens/s"
+ROW = 656
+
+
+def workloads():
+    from sparse_mla_attention_03_gb300 import inputs
+    return {
+        "prefill16k": dict(name="prefill_T1024_H64_ctx16384_k512+k1024", kind="prefill", bound="tensor",
+                           parts=[("k512", lambda s: inputs.prefill_16k(512, seed=s)),
+                                  ("k1024", lambda s: inputs.prefill_16k(1024, seed=s))]),
+        "fewhead": dict(name="fewhead_prefill_T8192_H8_ctx32768_k640_ld1024_ragged", kind="prefill",
+                        bound="hbm", parts=[("all", lambda s: inputs.fewhead_prefill(seed=s))]),
+        "decode": dict(name="decode_64req_x2_H64_ctx32768_k2048_paged", kind="decode", bound="hbm",
+                       parts=[("all", lambda s: inputs.batched_decode(seed=s))]),
+        "large": dict(name="large_prefill_T4096_H128_ctx131072_k2048_neg0.1", kind="prefill", bound="tensor",
+                      parts=[("all", lambda s: inputs.large_prefill(seed=s))]),
+        "tiny": dict(name="tiny_prefill_T4_H8_ctx256_k64", kind="prefill", bound="hbm",
+                     parts=[("all", lambda s: inputs.tiny_prefill(seed=s))]),
+    }
+
+
+def valid_slots(wl):
+    """Number of valid (token, slot) pairs: the units the algorithmic work counts."""
+    import numpy as np
+    idx = wl.indices.numpy()[:, :wl.topk].astype(np.int64)
+    T = idx.shape[0]
+    lens = np.full(T, wl.topk) if wl.topk_length is None else np.clip(wl.topk_length.numpy(), 0, wl.topk)
+    inlen = np.arange(wl.topk)[None, :] < lens[:, None]
+    if wl.block_table is None:
+        ok = inlen & (idx >= 0) & (idx < wl.num_pages * 64)
+    else:
+        ok = inlen & (idx >= 0) & (idx // 64 < wl.block_table.shape[1])
+    return int(ok.sum())
+
+
+def work_of(wl):
+    v = valid_slots(wl)
+    T, H = wl.T, wl.H
+    flops = 2.0 * H * (576 + 512) * v
+    gather = v * ROW
+    io = T * H * (576 * 2 + 512 * 2 + 4) + T * wl.topk * 4
+    return dict(valid=v, flops=flops, bytes=gather + io, gather_bytes=gather)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], tflops=d["bf16_tflops"], tflops_sus=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, tflops=1900.0, tflops_sus=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------------------------------------ oracle
+def _oracle_chunk(args):
+    import numpy as np
+    import oracle.sparse_mla_oracle as O
+    (q, kv, idx, topk, sm, tl, sink, bt, tpr, toks) = args
+    O.sparse_mla_forward(q, kv, idx, topk, sm, topk_length=tl, attn_sink=sink, block_table=bt,
+                         tokens_per_req=tpr, tokens=toks, q_selected=True)
+    return len(toks)
+
+
+def oracle_time(wl, n_tokens, cores):
+    """Oracle wall time on n_tokens tokens spread over `cores` spawn processes."""
+    import numpy as np
+    import torch
+    toks = np.arange(min(n_tokens, wl.T))
+    chunks = [c for c in np.array_split(toks, cores) if len(c)]
+    kv = wl.kv.numpy()
+    idx = wl.indices.numpy()
+    tl = None if wl.topk_length is None else wl.topk_length.numpy()
+    sink = None if wl.attn_sink is None else wl.attn_sink.numpy().astype(np.float64)
+    bt = None if wl.block_table is None else wl.block_table.numpy()
+    jobs = [(wl.q[torch.as_tensor(c)].to(torch.float64).numpy(), kv, idx, wl.topk, wl.sm_scale, tl, sink, bt,
+             wl.tokens_per_req, c) for c in chunks]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(len(jobs), initializer=_pin_threads) as pool:
+        pool.map(_oracle_chunk, jobs[:1])  # warm the workers' imports
+        t0 = time.perf_counter()
+        n = sum(pool.map(_oracle_chunk, jobs))
+        dt = time.perf_counter() - t0
+    return n, dt
+
+
+def _pin_threads():
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------------------------------------------ runs
+def make_call(kind, binding, d, wl, out, lse, ws, num_splits):
+    if kind == "prefill":
+        def call(stream=None):
+            binding.sparse_mla_prefill(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
+                                       topk_length=d["topk_length"], attn_sink=d["attn_sink"],
+                                       block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
+                                       out=out, lse=lse, stream=stream)
+    else:
+        def call(stream=None):
+            binding.sparse_mla_decode(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
+                                      topk_length=d["topk_length"], attn_sink=d["attn_sink"],
+                                      block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
+                                      num_splits=num_splits, workspace=ws, out=out, lse=lse, stream=stream)
+    return call
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from sparse_mla_attention_03_gb300 import binding
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    binding.load()
+    spec = workloads()[args.workload]
+    peaks = load_peaks()
+    parts = []
+    for tag, mk in spec["parts"]:
+        wl = mk(args.seed + rank)
+        d = {k: (None if getattr(wl, k) is None else getattr(wl, k).to(dev))
+             for k in ("q", "kv", "indices", "topk_length", "attn_sink", "block_table")}
+        out = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device=dev)
+        ws = None
+        if spec["kind"] == "decode":
+            ws = torch.empty(max(256, binding.decode_workspace_size(wl.T, wl.H, wl.topk, args.num_splits)),
+                             dtype=torch.uint8, device=dev)
+        call = make_call(spec["kind"], binding, d, wl, out, lse, ws, args.num_splits)
+        parts.append(dict(tag=tag, wl=wl, d=d, out=out, lse=lse, ws=ws, call=call, work=work_of(wl)))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_part = 2 if spec["kind"] == "decode" else 1
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        for p in parts:
+            p["call"]()
+    barrier()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
+          for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)
+            for j, p in enumerate(parts):
+                ev[s][j][0].record(stream)
+                p["call"]()
+                ev[s][j][1].record(stream)
+        barrier()
+        wall = time.perf_counter() - t0
+    per_part_ms = [[ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps)] for j in range(len(parts))]
+    step_ms = [sum(per_part_ms[j][s] for j in range(len(parts))) for s in range(args.steps)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens_per_step = sum(p["wl"].T for p in parts)
+    value = tokens_per_step * args.steps * world / (total_ms / 1e3)
+
+    # roofline of the dominant kernel (the attention kernel; for decode the split kernel dominates)
+    flops = sum(p["work"]["flops"] for p in parts)
+    nbytes = sum(p["work"]["bytes"] for p in parts)
+    avg_step_s = total_ms / args.steps / 1e3
+    if spec["bound"] == "tensor":
+        achieved = flops / avg_step_s / 1e12
+        roof = dict(bound="tensor", achieved=round(achieved, 2), peak=peaks["tflops"], unit="TFLOP/s",
+                    frac=round(achieved / peaks["tflops"], 4), traffic=None,
+                    peak_source=f"{peaks['src']} bf16 dense burst (fp16 operands run at the same rate)")
+    else:
+        achieved = nbytes / avg_step_s / 1e9
+        roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm"], unit="GB/s",
+                    frac=round(achieved / peaks["hbm"], 4), traffic=None,
+                    peak_source=f"{peaks['src']} HBM copy bandwidth")
+    roof["per_launch"] = {p["tag"]: dict(ms=round(statistics.mean(per_part_ms[j]), 4),
+                                         tflops=round(p["work"]["flops"] / (statistics.mean(per_part_ms[j]) / 1e3) / 1e12, 2),
+                                         gbs=round(p["work"]["bytes"] / (statistics.mean(per_part_ms[j]) / 1e3) / 1e9, 1))
+                          for j, p in enumerate(parts)}
+
+    e2e = run_e2e(args, parts, dev, stream, world)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8e4m3 KV / bf16 q in; f16 MMA operands, f32 accumulate; bf16 out",
+        "data": "synthetic (seeded numpy PCG64; no dataset or weights involved)",
+        "config": {"workload": spec["name"], "global_batch_tokens": tokens_per_step * world,
+                   "parallelism": f"dp{world} (independent token shards, no collective)",
+                   "l2": "flushed between steps (256 MiB write)", "seed": args.seed,
+                   "num_splits": args.num_splits if spec["kind"] == "decode" else None},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": args.steps * len(parts) * launches_per_part,
+        "clocks": clk.summary(),
+        "wall_s": round(wall, 3),
+    }
+    return line, parts
+
+
+def run_e2e(args, parts, dev, stream, world):
+    import torch
+    hosts = []
+    for p in parts:
+        wl = p["wl"]
+        hq = wl.q.pin_memory()
+        hi = wl.indices.pin_memory()
+        htl = None if wl.topk_length is None else wl.topk_length.pin_memory()
+        ho = torch.empty(p["out"].shape, dtype=p["out"].dtype).pin_memory()
+        hl = torch.empty(p["lse"].shape, dtype=p["lse"].dtype).pin_memory()
+        hosts.append((hq, hi, htl, ho, hl))
+    steps = max(1, min(args.steps, 20))
+    h2d = sum(h[0].numel() * 2 + h[1].numel() * 4 + (0 if h[2] is None else h[2].numel() * 4) for h in hosts)
+    d2h = sum(h[3].numel() * 2 + h[4].numel() * 4 for h in hosts)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(steps):
+        for p, (hq, hi, htl, ho, hl) in zip(parts, hosts):
+            p["d"]["q"].copy_(hq, non_blocking=True)
+            p["d"]["indices"].copy_(hi, non_blocking=True)
+            if htl is not None:
+                p["d"]["topk_length"].copy_(htl, non_blocking=True)
+            p["call"]()
+            ho.copy_(p["out"], non_blocking=True)
+            hl.copy_(p["lse"], non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(end)
+    tokens = sum(p["wl"].T for p in parts) * steps * world
+    return {"value": round(tokens / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def cpu_baseline(parts_or_wls, budget_tokens):
+    cores = min(host_cores(), 32)
+    n_tot, t_tot = 0, 0.0
+    descs = []
+    for wl in parts_or_wls:
+        n, dt = oracle_time(wl, budget_tokens, cores)
+        n_tot += n
+        t_tot += dt
+        descs.append(f"{wl.name}: first {n} tokens")
+    return {"value": round(n_tot / t_tot, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "; ".join(descs) + f" (fp64 numpy oracle, {cores} spawn processes, {t_tot:.1f} s)"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded token sample."""
+    spec = workloads()[args.workload]
+    wls = [mk(args.seed) for _, mk in spec["parts"]]
+    budget = args.ref_tokens
+    cores = min(host_cores(), 32)
+    times, toks = [], 0
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        for wl in wls:
+            oracle_time(wl, min(budget, cores), cores)
+    for _ in range(args.steps):
+        t = 0.0
+        for wl in wls:
+            n, dt = oracle_time(wl, budget, cores)
+            t += dt
+            toks += n
+        times.append(t)
+    total = sum(times)
+    value = toks / total
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy PCG64)",
+            "config": {"workload": spec["name"], "sample_tokens_per_part": budget},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"first {budget} tokens of each part per step"},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["prefill16k", "fewhead", "decode", "large", "tiny"],
+                    default="prefill16k")
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample per part for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=128, help="oracle sample per part per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line, parts = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if args.no_cpu_baseline:
+            line["cpu_baseline"] = None
+        else:
+            line["cpu_baseline"] = cpu_baseline([p["wl"] for p in parts], args.cpu_tokens)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * sparse_mla.h -- C ABI of libsparse_mla.so: sparse MLA attention forward
+ * (prefill and decode) for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  For each query token t and head h, over the valid slots j
+ * of the token's index row (see "Slots" below):
+ *
+ *   s_j      = sm_scale * < q[t,h,0:576], K[row_j] >
+ *   m        = max_j s_j,   l = sum_j exp(s_j - m)
+ *   out[t,h] = sum_j exp(s_j - m) V[row_j] / (l + exp(attn_sink[h] - m))   (bf16)
+ *   lse[t,h] = m + log(l)                                                  (fp32)
+ *
+ * with K[r] the 576-vector of cache row r dequantised (512 e4m3 codes times
+ * their per-128 fp32 scale, then 64 bf16 rope values) and V[r] = K[r][0:512].
+ * Sources: FlashInfer PR #4802 "Refactor Sparse MLA SM120" (review note on the
+ * DSv3.2 per-token KV layout: [0:512) e4m3, [512:528) 4 x fp32 scale, one per
+ * 128-element tile, [528:656) 64 x bf16 rope; d_v == d_nope per its Summary;
+ * page block 64; index row stride taken from the tensor; zero-token decode),
+ * vLLM PR #57673 "[Perf][DSv4.1] Native-head Triton sparse MLA for SM90
+ * few-head prefill" (Test Plan / Test Result: attn_sink, topk_length,
+ * non-contiguous q/out views written in place), and the AppMana
+ * forks-flash-mla-ampere-dsv4 releases page ("decode H6: warp-wide combine",
+ * split-K decode merged by LSE).
+ *
+ * Readings where the pages are silent: attn_sink[h] is a logit in the units
+ * of s_j that adds exp(attn_sink[h]) to the denominator only (NULL = no sink);
+ * lse excludes the sink and uses the natural log; a token with no valid slot
+ * gets out = 0 and lse = -inf.
+ *
+ * Slots.  Slot j of token t (j < topk) is valid iff
+ *   j < clamp(topk_length[t], 0, topk)   (topk_length NULL: topk), and
+ *   its index i = indices[t*idx_stride_t + j] resolves to a cache row:
+ *     flat  (block_table NULL): row = i, 0 <= i < num_pages*64;
+ *     paged: r = t / tokens_per_req (< bt_rows), page = i / 64 (< bt_cols),
+ *            p = block_table[r*bt_stride + page] (0 <= p < num_pages),
+ *            row = p*64 + i % 64.
+ * -1 is padding.  Any other index that does not resolve is masked like -1 and
+ * sets bit SMLA_ERRF_INDEX_RANGE in the device error word.  Index entries at
+ * or past topk_length are not read.
+ *
+ * Conventions for every call:
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     keeps none of them after the call returns and never frees them.
+ *   - Calls are asynchronous on the given stream (0 = legacy default stream).
+ *     They do not synchronise and do not allocate device memory.
+ *   - T == 0 returns SMLA_OK without launching anything.
+ *   - Return codes: SMLA_OK, SMLA_ERR_INVALID (bad argument: the call did
+ *     nothing), SMLA_ERR_UNSUPPORTED, SMLA_ERR_CUDA (a launch failed).
+ *     sparse_mla_last_error() gives a message for the calling thread.
+ *   - Range of the cache values: the kernels hold dequantised values in fp16,
+ *     so every |e4m3 * scale| must be at most 65504 (scales at most 128).
+ */
+#ifndef SPARSE_MLA_H_
+#define SPARSE_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* smla_stream_t;
+
+enum {
+  SMLA_OK = 0,
+  SMLA_ERR_INVALID = 1,
+  SMLA_ERR_UNSUPPORTED = 2,
+  SMLA_ERR_CUDA = 3,
+  SMLA_ERR_DEVICE = 4
+};
+
+/* Bits of the device error word (sparse_mla_get_error_word). */
+enum {
+  SMLA_ERRF_INDEX_RANGE = 1, /* an index other than -1 did not resolve (masked) */
+  SMLA_ERRF_TIMEOUT = 2,     /* a bounded in-kernel wait gave up; outputs invalid */
+  SMLA_ERRF_SCALE_RANGE = 4  /* a cache row scale above 128 was seen */
+};
+
+#define SMLA_D_QK 576
+#define SMLA_D_V 512
+#define SMLA_ROW_BYTES 656
+#define SMLA_PAGE 64
+#define SMLA_MAX_HEADS 128
+#define SMLA_MAX_SPLITS 64
+
+/*
+ * Arguments shared by prefill and decode.  Strides are in ELEMENTS of the
+ * pointed-to type.
+ *
+ *  q            bf16 [T, H, 576]: head stride 576, token stride q_stride_t
+ *               (>= H*576; a view into a wider buffer is fine).
+ *  kv           uint8 [num_pages, 64, 656], contiguous rows, 16-byte aligned.
+ *  block_table  int32 [bt_rows, >= bt_cols] with row stride bt_stride, or
+ *               NULL for flat row ids.  tokens_per_req query tokens share a
+ *               block-table row (decode: request r owns tokens
+ *               r*tokens_per_req ... ; needs bt_rows*tokens_per_req >= T).
+ *  indices      int32 [T, >= topk]: row stride idx_stride_t (>= topk), last
+ *               dimension contiguous.
+ *  topk_length  int32 [T] or NULL.
+ *  attn_sink    fp32 [H] or NULL.
+ *  out          bf16 [T, H, 512]: head stride 512, token stride out_stride_t
+ *               (>= H*512, multiple of 4), 8-byte aligned; written in place.
+ *  lse          fp32 [T, H]: token stride lse_stride_t (>= H).
+ *  H in [1, 128]; T >= 0; topk >= 1.
+ */
+typedef struct smla_args {
+  const void* q;
+  int64_t q_stride_t;
+  const uint8_t* kv;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int32_t bt_rows;
+  int32_t bt_cols;
+  int32_t tokens_per_req;
+  int32_t topk;
+  const int32_t* indices;
+  int64_t idx_stride_t;
+  const int32_t* topk_length;
+  const float* attn_sink;
+  float sm_scale;
+  int32_t T;
+  int32_t H;
+  int32_t reserved0; /* must be 0 */
+  void* out;
+  int64_t out_stride_t;
+  float* lse;
+  int64_t lse_stride_t;
+} smla_args;
+
+/*
+ * Prefill: one pass over every token's selected rows, with gather, dequant,
+ * QK^T, sink softmax, PV and the epilogue fused per token (the fused path of
+ * the AppMana releases page, "Remove the legacy staged sparse-MLA prefill
+ * kernel": no materialised gather).  H % 64 == 0 runs on the tcgen05/TMEM
+ * kernel; other head counts run at their native width on the warp-MMA kernel
+ * (vLLM PR #57673: no zero-padding of few heads to 64).
+ */
+int sparse_mla_prefill(const smla_args* args, smla_stream_t stream);
+
+/*
+ * Decode: the topk slots of each token are cut into num_splits contiguous
+ * chunks (multiples of 64 slots); each chunk is attended by its own CTA,
+ * which writes an fp32 partial (output normalised over its slots, sink-free,
+ * and its LSE) to the caller's workspace; a combine kernel then merges the
+ * partials with weights exp(lse_s - lse) and applies the sink (FlashInfer PR
+ * #4802, "Runner and CUDA graphs": split-K scratch owned by the caller; AppMana
+ * releases, "decode H6: warp-wide combine").
+ *
+ *  num_splits   0 = automatic, else 1..64 (reduced so that no split is empty
+ *               of slots: effective splits = ceil(topk / chunk)).
+ *  workspace    device memory, 256-byte aligned, at least
+ *               sparse_mla_decode_workspace_size(T, H, topk, num_splits)
+ *               bytes; its contents on entry do not matter.  Calls that share a
+ *               workspace must be ordered on one stream.
+ */
+int sparse_mla_decode(const smla_args* args, int32_t num_splits, void* workspace,
+                      size_t workspace_bytes, smla_stream_t stream);
+
+/*
+ * Workspace bytes that sparse_mla_decode needs for these sizes on the
+ * current device.  num_splits == 0 sizes for the automatic choice.  Returns 0
+ * for invalid sizes.  T == 0 needs no workspace (returns 0).
+ */
+size_t sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t topk,
+                                        int32_t num_splits);
+
+/* The split count sparse_mla_decode uses for num_splits (0 = automatic). */
+int32_t sparse_mla_decode_num_splits(int32_t T, int32_t H, int32_t topk, int32_t num_splits);
+
+/*
+ * Index handling only: rows_out[t*rows_stride_t + j] (int32, device) receives
+ * the physical cache row of slot j of token t, or -1 if the slot is invalid,
+ * for j < topk.  Runs the same device resolution routine as the attention
+ * kernels; used to check index handling bit for bit.
+ */
+int sparse_mla_resolve_rows(const smla_args* args, int32_t* rows_out, int64_t rows_stride_t,
+                            smla_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word (SMLA_ERRF_* bits) into *out_flags.
+ */
+int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* sparse_mla_last_error(void);
+
+/* ABI version (bumped on any change of this header). */
+int32_t sparse_mla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPARSE_MLA_H_ */

@@ -191,10 +191,11 @@ def attend_one(q_t, K, sm_scale, sink=None):
 
 def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
                        attn_sink=None, block_table=None, tokens_per_req=1,
-                       tokens=None):
+                       tokens=None, q_selected=False):
     """Sparse MLA forward for the selected tokens (all tokens by default).
 
-    ``q``: float64 ``[T, H, 576]`` (bf16 values widened exactly);
+    ``q``: float64 ``[T, H, 576]`` (bf16 values widened exactly), or only the
+    rows of ``tokens`` in that order when ``q_selected``;
     ``kv_cache``: uint8 ``[num_pages, 64, 656]`` (or ``[rows, 656]``);
     ``indices``: int ``[T, >= topk]``.  Returns float64 ``out [n_sel, H, 512]``
     and ``lse [n_sel, H]`` (natural log, sink excluded).
@@ -202,9 +203,12 @@ def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
     kv = np.asarray(kv_cache, dtype=np.uint8).reshape(-1, ROW_BYTES)
     num_pages = kv.shape[0] // PAGE_BLOCK
     q = np.asarray(q, dtype=np.float64)
-    T, H, D = q.shape
+    T = np.asarray(indices).shape[0]
+    _, H, D = q.shape
     assert D == D_QK
     sel = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    if q_selected:
+        assert q.shape[0] == sel.shape[0]
     rows = resolve_rows(indices, topk, num_pages, topk_length, block_table,
                         tokens_per_req, sel)
     out = np.zeros((sel.shape[0], H, D_V))
@@ -213,7 +217,7 @@ def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
     for i, t in enumerate(sel):
         r = rows[i]
         K = decode_rows(kv[r[r >= 0]])
-        out[i], lse[i] = attend_one(q[t], K, sm_scale, sink)
+        out[i], lse[i] = attend_one(q[i] if q_selected else q[t], K, sm_scale, sink)
     return out, lse
 
 

@@ -1,0 +1,251 @@
+// C ABI of libsparse_mla.so: argument validation, kernel choice and launches.
+// The operations themselves are defined in include/sparse_mla.h.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/sparse_mla.h"
+#include "smla_launch.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+// One error word per device; its address is looked up once per device.
+__device__ int g_error_word;
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_setup(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return fail(SMLA_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(cudaGetLastError()));
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    int* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_error_word);
+    if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    g_num_sms[dev] = sms;
+    g_err_ptr[dev] = ptr;
+  }
+  *dev_out = dev;
+  return SMLA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int validate(const smla_args* a) {
+  if (a == nullptr) return fail(SMLA_ERR_INVALID, "args is NULL");
+  if (a->T < 0) return fail(SMLA_ERR_INVALID, "T = %d < 0", a->T);
+  if (a->H < 1 || a->H > SMLA_MAX_HEADS) return fail(SMLA_ERR_INVALID, "H = %d not in [1, 128]", a->H);
+  if (a->topk < 1) return fail(SMLA_ERR_INVALID, "topk = %d < 1", a->topk);
+  if (a->reserved0 != 0) return fail(SMLA_ERR_INVALID, "reserved0 must be 0");
+  if (!(a->sm_scale == a->sm_scale) || a->sm_scale > 3.0e38f || a->sm_scale < -3.0e38f)
+    return fail(SMLA_ERR_INVALID, "sm_scale is not finite");
+  if (a->T == 0) return SMLA_OK;
+  if (!a->q || !a->indices || !a->out || !a->lse)
+    return fail(SMLA_ERR_INVALID, "q, indices, out and lse must be non-NULL");
+  if (a->num_pages < 0 || a->num_pages * SMLA_PAGE > 0x7FFFFFFFLL)
+    return fail(SMLA_ERR_INVALID, "num_pages = %lld out of range", (long long)a->num_pages);
+  if (a->num_pages > 0 && !a->kv) return fail(SMLA_ERR_INVALID, "kv is NULL");
+  if (a->kv && !aligned(a->kv, 16)) return fail(SMLA_ERR_INVALID, "kv must be 16-byte aligned");
+  if (a->q_stride_t < (int64_t)a->H * SMLA_D_QK)
+    return fail(SMLA_ERR_INVALID, "q_stride_t = %lld < H*576", (long long)a->q_stride_t);
+  if (a->out_stride_t < (int64_t)a->H * SMLA_D_V || a->out_stride_t % 4 != 0)
+    return fail(SMLA_ERR_INVALID, "out_stride_t = %lld must be >= H*512 and a multiple of 4",
+                (long long)a->out_stride_t);
+  if (a->lse_stride_t < a->H) return fail(SMLA_ERR_INVALID, "lse_stride_t < H");
+  if (a->idx_stride_t < a->topk) return fail(SMLA_ERR_INVALID, "idx_stride_t < topk");
+  if (!aligned(a->q, 2) || !aligned(a->out, 8) || !aligned(a->lse, 4) || !aligned(a->indices, 4))
+    return fail(SMLA_ERR_INVALID, "misaligned q/out/lse/indices (need 2/8/4/4 bytes)");
+  if (a->topk_length && !aligned(a->topk_length, 4)) return fail(SMLA_ERR_INVALID, "misaligned topk_length");
+  if (a->attn_sink && !aligned(a->attn_sink, 4)) return fail(SMLA_ERR_INVALID, "misaligned attn_sink");
+  if (a->block_table) {
+    if (a->tokens_per_req < 1) return fail(SMLA_ERR_INVALID, "tokens_per_req < 1");
+    if (a->bt_cols < 1 || a->bt_stride < a->bt_cols || a->bt_rows < 1)
+      return fail(SMLA_ERR_INVALID, "bad block table shape (rows %d, cols %d, stride %lld)", a->bt_rows,
+                  a->bt_cols, (long long)a->bt_stride);
+    if ((int64_t)a->bt_rows * a->tokens_per_req < a->T)
+      return fail(SMLA_ERR_INVALID, "block table has %d rows for %d tokens at %d tokens/request", a->bt_rows,
+                  a->T, a->tokens_per_req);
+    if (!aligned(a->block_table, 4)) return fail(SMLA_ERR_INVALID, "misaligned block_table");
+  }
+  return SMLA_OK;
+}
+
+smla::KParams make_params(const smla_args* a, int dev) {
+  smla::KParams p;
+  memset(&p, 0, sizeof(p));
+  p.q = static_cast<const __nv_bfloat16*>(a->q);
+  p.q_stride_t = a->q_stride_t;
+  p.kv = a->kv;
+  p.num_pages = a->num_pages;
+  p.block_table = a->block_table;
+  p.bt_stride = a->bt_stride;
+  p.bt_rows = a->bt_rows;
+  p.bt_cols = a->bt_cols;
+  p.tokens_per_req = a->block_table ? a->tokens_per_req : 1;
+  p.indices = a->indices;
+  p.idx_stride_t = a->idx_stride_t;
+  p.topk = a->topk;
+  p.topk_length = a->topk_length;
+  p.attn_sink = a->attn_sink;
+  p.sm_scale = a->sm_scale;
+  p.T = a->T;
+  p.H = a->H;
+  p.out = static_cast<__nv_bfloat16*>(a->out);
+  p.out_stride_t = a->out_stride_t;
+  p.lse = a->lse;
+  p.lse_stride_t = a->lse_stride_t;
+  p.num_splits = 1;
+  p.split_len = ((a->topk + 63) / 64) * 64;
+  p.err = g_err_ptr[dev];
+  return p;
+}
+
+// Decode split choice.  An explicit request is honoured up to the number of
+// 64-slot chunks; the automatic choice keeps splitting while the grid is below
+// two waves and every split still holds at least 4 chunks.
+int splits_for(int T, int H, int topk, int num_splits, int num_sms) {
+  const int chunks = (topk + 63) / 64;
+  int S;
+  if (num_splits > 0) {
+    S = num_splits < chunks ? num_splits : chunks;
+  } else {
+    const int hpc = smla::mma_heads_per_cta(H);
+    const int64_t base = (int64_t)T * ((H + hpc - 1) / hpc);
+    const int64_t target = 2LL * (num_sms > 0 ? num_sms : 148);
+    S = 1;
+    while (base * (S * 2) <= target && chunks / (S * 2) >= 4 && S * 2 <= SMLA_MAX_SPLITS) S *= 2;
+  }
+  if (S < 1) S = 1;
+  // effective count: chunks per split rounded up, then splits that hold slots
+  const int per = (chunks + S - 1) / S;
+  return (chunks + per - 1) / per;
+}
+
+size_t ws_bytes(int64_t T, int64_t H, int64_t S) {
+  const size_t o = (size_t)(T * H * S * SMLA_D_V) * sizeof(float);
+  const size_t l = (size_t)(T * H * S) * sizeof(float);
+  return ((o + 255) / 256) * 256 + ((l + 255) / 256) * 256;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t sparse_mla_abi_version(void) { return 1; }
+
+const char* sparse_mla_last_error(void) { return g_last_error; }
+
+int sparse_mla_prefill(const smla_args* a, smla_stream_t stream) {
+  g_last_error[0] = 0;
+  int rc = validate(a);
+  if (rc != SMLA_OK) return rc;
+  if (a->T == 0) return SMLA_OK;
+  int dev;
+  if ((rc = device_setup(&dev)) != SMLA_OK) return rc;
+  smla::KParams p = make_params(a, dev);
+  cudaError_t e = smla::launch_mma(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  return SMLA_OK;
+}
+
+int32_t sparse_mla_decode_num_splits(int32_t T, int32_t H, int32_t topk, int32_t num_splits) {
+  if (T < 0 || H < 1 || H > SMLA_MAX_HEADS || topk < 1 || num_splits < 0 || num_splits > SMLA_MAX_SPLITS) return 0;
+  int sms = 0;
+  if (num_splits == 0) {
+    int dev;
+    if (device_setup(&dev) != SMLA_OK) return 0;
+    sms = g_num_sms[dev];
+  }
+  return splits_for(T, H, topk, num_splits, sms);
+}
+
+size_t sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t topk, int32_t num_splits) {
+  if (T <= 0) return 0;
+  const int S = sparse_mla_decode_num_splits(T, H, topk, num_splits);
+  if (S <= 0) return 0;
+  return ws_bytes(T, H, S);
+}
+
+int sparse_mla_decode(const smla_args* a, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                      smla_stream_t stream) {
+  g_last_error[0] = 0;
+  int rc = validate(a);
+  if (rc != SMLA_OK) return rc;
+  if (num_splits < 0 || num_splits > SMLA_MAX_SPLITS)
+    return fail(SMLA_ERR_INVALID, "num_splits = %d not in [0, 64]", num_splits);
+  if (a->T == 0) return SMLA_OK;  // zero tokens: nothing to launch
+  int dev;
+  if ((rc = device_setup(&dev)) != SMLA_OK) return rc;
+  const int S = splits_for(a->T, a->H, a->topk, num_splits, g_num_sms[dev]);
+  const size_t need = ws_bytes(a->T, a->H, S);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(SMLA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+  if (!aligned(workspace, 256)) return fail(SMLA_ERR_INVALID, "workspace must be 256-byte aligned");
+  smla::KParams p = make_params(a, dev);
+  const int chunks = (a->topk + 63) / 64;
+  p.num_splits = S;
+  p.split_len = ((chunks + S - 1) / S) * 64;
+  const size_t o_bytes = (size_t)a->T * a->H * S * SMLA_D_V * sizeof(float);
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = smla::launch_mma(p, st);
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode split launch: %s", cudaGetErrorString(e));
+  e = smla::launch_combine(p, st);
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode combine launch: %s", cudaGetErrorString(e));
+  return SMLA_OK;
+}
+
+int sparse_mla_resolve_rows(const smla_args* a, int32_t* rows_out, int64_t rows_stride_t, smla_stream_t stream) {
+  g_last_error[0] = 0;
+  int rc = validate(a);
+  if (rc != SMLA_OK) return rc;
+  if (a->T == 0) return SMLA_OK;
+  if (rows_out == nullptr || rows_stride_t < a->topk)
+    return fail(SMLA_ERR_INVALID, "rows_out is NULL or rows_stride_t < topk");
+  int dev;
+  if ((rc = device_setup(&dev)) != SMLA_OK) return rc;
+  smla::KParams p = make_params(a, dev);
+  cudaError_t e = smla::launch_resolve(p, rows_out, rows_stride_t, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "resolve launch: %s", cudaGetErrorString(e));
+  return SMLA_OK;
+}
+
+int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags) {
+  g_last_error[0] = 0;
+  if (out_flags == nullptr) return fail(SMLA_ERR_INVALID, "out_flags is NULL");
+  int dev;
+  int rc = device_setup(&dev);
+  if (rc != SMLA_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int));
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "read error word: %s", cudaGetErrorString(e));
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "clear error word: %s", cudaGetErrorString(e));
+  *out_flags = v;
+  return SMLA_OK;
+}
+
+}  // extern "C"

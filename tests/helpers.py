@@ -25,15 +25,11 @@ def oracle_for(wl, tokens=None, indices=None, topk=None, topk_length="wl", attn_
     sk = wl.attn_sink if attn_sink == "wl" else attn_sink
     bt = None if wl.block_table is None else wl.block_table.numpy()
     sel = None if tokens is None else np.asarray(tokens)
-    if sel is not None:
-        # q was already sliced; pass positions so indices/lengths/requests line up
-        full_q = np.zeros((wl.T, wl.H, 576))
-        full_q[sel] = q
-        q = full_q
     return O.sparse_mla_forward(q, wl.kv.numpy(), idx, topk or wl.topk, wl.sm_scale,
                                 topk_length=None if tl is None else tl.numpy(),
                                 attn_sink=None if sk is None else sk.numpy().astype(np.float64),
-                                block_table=bt, tokens_per_req=wl.tokens_per_req, tokens=sel)
+                                block_table=bt, tokens_per_req=wl.tokens_per_req, tokens=sel,
+                                q_selected=sel is not None)
 
 
 def assert_close(out_gpu, lse_gpu, out_ref, lse_ref, tag=""):

@@ -1,0 +1,93 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every symbol
+the header declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_mla_attention_03_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(binding.LIB_PATH):
+        from sparse_mla_attention_03_gb300 import build
+        build.build()
+    return binding.load()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "sparse_mla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sparse_mla_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert len(names) >= 8, names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(binding.SYMBOLS), (set(names) ^ set(binding.SYMBOLS))
+
+
+def test_struct_layout_matches_header():
+    assert ctypes.sizeof(binding.SmlaArgs) == 144
+    assert binding.SmlaArgs.out.offset == 112
+    assert binding.SmlaArgs.sm_scale.offset == 96
+
+
+def _args(**kw):
+    a = binding.SmlaArgs()
+    a.q, a.q_stride_t = 0x1000, 8 * 576
+    a.kv, a.num_pages = 0x2000, 4
+    a.topk, a.indices, a.idx_stride_t = 64, 0x3000, 64
+    a.sm_scale, a.T, a.H = 0.04, 4, 8
+    a.out, a.out_stride_t = 0x4000, 8 * 512
+    a.lse, a.lse_stride_t = 0x5000, 8
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("bad", [
+    dict(H=0), dict(H=129), dict(topk=0), dict(T=-1), dict(q_stride_t=100), dict(out_stride_t=8 * 512 + 2),
+    dict(lse_stride_t=4), dict(idx_stride_t=10), dict(q=0), dict(kv=0x2001), dict(out=0x4002),
+    dict(reserved0=1), dict(sm_scale=float("nan")), dict(num_pages=-1),
+    dict(block_table=0x6000, bt_rows=1, bt_cols=8, bt_stride=8, tokens_per_req=2),  # 2 tokens/row x 1 row < 4
+    dict(block_table=0x6000, bt_rows=4, bt_cols=8, bt_stride=4, tokens_per_req=1),  # stride < cols
+])
+def test_invalid_arguments_rejected_without_cuda(lib, bad):
+    a = _args(**bad)
+    rc = lib.sparse_mla_prefill(ctypes.byref(a), None)
+    assert rc == binding.SMLA_ERR_INVALID
+    assert lib.sparse_mla_last_error().decode()
+    rc = lib.sparse_mla_decode(ctypes.byref(a), 0, None, 0, None)
+    assert rc == binding.SMLA_ERR_INVALID
+
+
+def test_zero_tokens_is_a_no_op(lib):
+    a = _args(T=0, q=0, out=0, lse=0, indices=0)
+    assert lib.sparse_mla_prefill(ctypes.byref(a), None) == binding.SMLA_OK
+    assert lib.sparse_mla_decode(ctypes.byref(a), 0, None, 0, None) == binding.SMLA_OK
+    assert lib.sparse_mla_decode_workspace_size(0, 8, 64, 0) == 0
+
+
+def test_null_args_and_bad_splits(lib):
+    assert lib.sparse_mla_prefill(None, None) == binding.SMLA_ERR_INVALID
+    a = _args()
+    assert lib.sparse_mla_decode(ctypes.byref(a), 65, None, 0, None) == binding.SMLA_ERR_INVALID
+    assert lib.sparse_mla_decode(ctypes.byref(a), -1, None, 0, None) == binding.SMLA_ERR_INVALID
+
+
+def test_explicit_split_arithmetic(lib):
+    # explicit splits need no device: effective count never exceeds the 64-slot chunks
+    assert lib.sparse_mla_decode_num_splits(128, 64, 2048, 8) == 8
+    assert lib.sparse_mla_decode_num_splits(128, 64, 2048, 64) == 32
+    assert lib.sparse_mla_decode_num_splits(4, 8, 100, 3) == 2
+    assert lib.sparse_mla_decode_num_splits(4, 8, 640, 3) == 3
+    ws = lib.sparse_mla_decode_workspace_size(128, 64, 2048, 8)
+    assert ws == 128 * 64 * 8 * 512 * 4 + 128 * 64 * 8 * 4
+    assert lib.sparse_mla_abi_version() == 1

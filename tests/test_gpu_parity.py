@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small cases run the oracle on every token (several 64-row tiles plus a ragged
+tail); the full-size workloads run the oracle on a seeded sample of tokens.
+Index handling is compared bit for bit through sparse_mla_resolve_rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.sparse_mla_oracle as O
+from sparse_mla_attention_03_gb300 import binding, inputs
+from tests.helpers import assert_close, oracle_for, sample_tokens, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(wl, **kw):
+    d = to_dev(wl)
+    return binding.sparse_mla_prefill(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
+                                      topk_length=d["topk_length"], attn_sink=d["attn_sink"],
+                                      block_table=d["block_table"], tokens_per_req=wl.tokens_per_req, **kw)
+
+
+def run_decode(wl, num_splits=0, **kw):
+    d = to_dev(wl)
+    return binding.sparse_mla_decode(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
+                                     topk_length=d["topk_length"], attn_sink=d["attn_sink"],
+                                     block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
+                                     num_splits=num_splits, **kw)
+
+
+@pytest.fixture(autouse=True)
+def _lib(cuda_lib):
+    binding.get_error_word()  # clear
+    yield
+
+
+# ----------------------------------------------------------------------------- small, full oracle
+def test_tiny_workload_prefill_and_decode():
+    wl = inputs.tiny_prefill()
+    ref = oracle_for(wl)
+    out, lse = run_prefill(wl)
+    torch.cuda.synchronize()
+    assert_close(out, lse, *ref, tag="tiny prefill")
+    for s in (0, 1, 2):
+        out, lse = run_decode(wl, num_splits=s)
+        assert_close(out, lse, *ref, tag=f"tiny decode S={s}")
+    assert binding.get_error_word() == 0
+
+
+@pytest.mark.parametrize("H", [1, 5, 8, 16, 24, 64, 128])
+@pytest.mark.parametrize("sink", ["normal", None])
+def test_small_prefill_heads(H, sink):
+    wl = inputs.make_prefill(f"small_H{H}", T=5, H=H, ctx=2048, topk=200, seed=H, sink=sink,
+                             neg_prob=0.15)
+    ref = oracle_for(wl)
+    out, lse = run_prefill(wl)
+    assert_close(out, lse, *ref, tag=f"H={H} sink={sink}")
+
+
+@pytest.mark.parametrize("H", [8, 64])
+def test_ragged_topk_length_and_strided_index_view(H):
+    wl = inputs.make_prefill("ragged", T=7, H=H, ctx=4096, topk=320, seed=21, ld=512, ragged=True)
+    wl.topk_length[0] = 0
+    wl.topk_length[1] = 1
+    wl.topk_length[2] = 320
+    wl.topk_length[3] = 65
+    ref = oracle_for(wl)
+    out, lse = run_prefill(wl)
+    assert_close(out, lse, *ref, tag="ragged")
+    lse_h = lse.cpu().numpy()
+    assert np.all(np.isneginf(lse_h[0])) and np.all(out[0].float().cpu().numpy() == 0)
+
+
+@pytest.mark.parametrize("H", [8, 64])
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 8, 32])
+def test_decode_split_invariance_paged(H, S):
+    wl = inputs.make_decode("dec_small", n_req=3, tokens_per_req=2, H=H, ctx_per_req=4096, topk=2048,
+                            seed=31 + S)
+    ref = oracle_for(wl)
+    out, lse = run_decode(wl, num_splits=S)
+    assert_close(out, lse, *ref, tag=f"decode H={H} S={S}")
+
+
+def test_noncontiguous_views_written_in_place():
+    # q[:, :8] / out[:, :8] views into width-64 buffers; index rows from a width-1024 buffer
+    wl = inputs.make_prefill("views", T=6, H=8, ctx=2048, topk=192, seed=41, ld=1024)
+    d = to_dev(wl)
+    qbuf = torch.randn(6, 64, 576, device="cuda").to(torch.bfloat16)
+    qbuf[:, :8] = d["q"]
+    obuf = torch.full((6, 64, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+    lbuf = torch.full((6, 64), 7.0, dtype=torch.float32, device="cuda")
+    out, lse = binding.sparse_mla_prefill(qbuf[:, :8], d["kv"], d["indices"], wl.sm_scale, topk=192,
+                                          attn_sink=d["attn_sink"], out=obuf[:, :8], lse=lbuf[:, :8])
+    assert out.data_ptr() == obuf.data_ptr()
+    ref = oracle_for(wl)
+    assert_close(obuf[:, :8], lbuf[:, :8], *ref, tag="views")
+    assert torch.all(obuf[:, 8:] == 7.0) and torch.all(lbuf[:, 8:] == 7.0)
+
+
+def test_single_valid_index_and_empty_rows():
+    wl = inputs.make_prefill("single", T=4, H=16, ctx=1024, topk=128, seed=51)
+    idx = torch.full((4, 128), -1, dtype=torch.int32)
+    idx[0, 77] = 5
+    idx[1, 0] = 1023
+    wl.indices = idx  # rows 2, 3 have no valid slot
+    ref = oracle_for(wl)
+    out, lse = run_prefill(wl)
+    assert_close(out, lse, *ref, tag="single")
+    out, lse = run_decode(wl, num_splits=2)
+    assert_close(out, lse, *ref, tag="single decode")
+
+
+def test_index_resolution_bit_exact_flat_and_paged():
+    wl = inputs.make_prefill("res", T=9, H=8, ctx=1024, topk=96, seed=61, ld=130, ragged=True)
+    idx = wl.indices.clone()
+    idx[0, :4] = torch.tensor([1024, -5, 0x7FFFFFFF, 1023], dtype=torch.int32)
+    wl.topk_length[0] = 96
+    d = to_dev(wl)
+    rows = binding.sparse_mla_resolve_rows(d["q"], d["kv"], idx.cuda(), topk=96,
+                                           topk_length=d["topk_length"]).cpu().numpy()
+    want = O.resolve_rows(idx.numpy(), 96, wl.num_pages, wl.topk_length.numpy())
+    np.testing.assert_array_equal(rows, want)
+    assert binding.get_error_word() & binding.ERRF_INDEX_RANGE
+    dec = inputs.make_decode("resp", n_req=4, tokens_per_req=2, H=8, ctx_per_req=1024, topk=64, seed=62)
+    didx = dec.indices.clone()
+    didx[1, 3] = 1024  # logical page 16 is outside the 16-column block-table row
+    dd = to_dev(dec)
+    rows = binding.sparse_mla_resolve_rows(dd["q"], dd["kv"], didx.cuda(), block_table=dd["block_table"],
+                                           tokens_per_req=2).cpu().numpy()
+    want = O.resolve_rows(didx.numpy(), 64, dec.num_pages, block_table=dec.block_table.numpy(),
+                          tokens_per_req=2)
+    np.testing.assert_array_equal(rows, want)
+    assert binding.get_error_word() & binding.ERRF_INDEX_RANGE
+
+
+def test_two_streams_match_one_stream():
+    wa = inputs.make_prefill("sa", T=16, H=8, ctx=2048, topk=256, seed=71)
+    wb = inputs.make_prefill("sb", T=16, H=64, ctx=2048, topk=256, seed=72)
+    ref_a, ref_b = run_prefill(wa), run_prefill(wb)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    da, db = to_dev(wa), to_dev(wb)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        oa = binding.sparse_mla_prefill(da["q"], da["kv"], da["indices"], wa.sm_scale, attn_sink=da["attn_sink"])
+    with torch.cuda.stream(s2):
+        ob = binding.sparse_mla_prefill(db["q"], db["kv"], db["indices"], wb.sm_scale, attn_sink=db["attn_sink"])
+    torch.cuda.synchronize()
+    assert torch.equal(oa[0], ref_a[0]) and torch.equal(oa[1], ref_a[1])
+    assert torch.equal(ob[0], ref_b[0]) and torch.equal(ob[1], ref_b[1])
+
+
+def test_zero_tokens():
+    wl = inputs.make_prefill("z", T=1, H=8, ctx=64, topk=8, seed=81)
+    d = to_dev(wl)
+    q0 = d["q"][:0]
+    out, lse = binding.sparse_mla_prefill(q0, d["kv"], d["indices"][:0], wl.sm_scale)
+    assert out.shape == (0, 8, 512)
+    out, lse = binding.sparse_mla_decode(q0, d["kv"], d["indices"][:0], wl.sm_scale)
+    assert lse.shape == (0, 8)
+
+
+def test_deterministic_repeat():
+    wl = inputs.make_prefill("det", T=8, H=64, ctx=4096, topk=512, seed=91)
+    a = run_prefill(wl)
+    b = run_prefill(wl)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+FULL = {
+    "prefill16k_k512": (lambda: inputs.prefill_16k(512), "prefill", 48),
+    "prefill16k_k1024": (lambda: inputs.prefill_16k(1024), "prefill", 48),
+    "fewhead": (inputs.fewhead_prefill, "prefill", 96),
+    "decode": (inputs.batched_decode, "decode", 48),
+    "large": (inputs.large_prefill, "prefill", 24),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_workload_sampled(name):
+    make, kind, n = FULL[name]
+    wl = make()
+    out, lse = (run_prefill(wl) if kind == "prefill" else run_decode(wl))
+    toks = sample_tokens(wl.T, n, seed=5, must=(0, wl.T - 1))
+    ref = oracle_for(wl, tokens=toks)
+    tt = torch.as_tensor(toks, device=out.device)
+    assert_close(out[tt], lse[tt], *ref, tag=name)
+    assert torch.isfinite(out).all()
+    assert binding.get_error_word() == 0
