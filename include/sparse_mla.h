@@ -185,6 +185,30 @@ int sparse_mla_resolve_rows(const smla_args* args, int32_t* rows_out, int64_t ro
  */
 int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags);
 
+/*
+ * Decode without any device allocation -- no counterpart on the pages; added
+ * for callers that cannot allocate device memory: a host engine that owns all
+ * device memory through its own pool and gives a library only tensors and a
+ * stream (cudaMalloc there fails or escapes the pool's accounting), or a
+ * latency-critical path where an allocation and its implicit synchronisation
+ * are not acceptable.  Same operation, kernels and results as
+ * sparse_mla_decode, but the split partials live in a fixed array compiled
+ * into the library (SMLA_NOALLOC_SCRATCH_BYTES per GPU, kept by every GPU
+ * that loads it until the process exits).  The caller still passes every
+ * input and output through args.
+ *  - Calls whose partials need more than SMLA_NOALLOC_SCRATCH_BYTES (see
+ *    sparse_mla_decode_workspace_size) are rejected with SMLA_ERR_INVALID.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, once per device); make that first call before any
+ *    stream capture begins.
+ *  - All calls on a device share the array, which keeps the last call's
+ *    contents: calls that overlap on the GPU (different streams, no ordering
+ *    between them) race.  Order them on one stream.
+ *  - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define SMLA_NOALLOC_SCRATCH_BYTES (64u << 20)
+int sparse_mla_decode_noalloc(const smla_args* args, int32_t num_splits, smla_stream_t stream);
+
 /* Message for the last failing call on this thread ("" if none). */
 const char* sparse_mla_last_error(void);
 

@@ -54,6 +54,7 @@ SYMBOLS = {
     "sparse_mla_decode_workspace_size": (ctypes.c_size_t, [ctypes.c_int32] * 4),
     "sparse_mla_decode_num_splits": (ctypes.c_int32, [ctypes.c_int32] * 4),
     "sparse_mla_resolve_rows": (ctypes.c_int, [_P, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
+    "sparse_mla_decode_noalloc": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_void_p]),
     "sparse_mla_get_error_word": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "sparse_mla_last_error": (ctypes.c_char_p, []),
     "sparse_mla_abi_version": (ctypes.c_int32, []),
@@ -201,6 +202,24 @@ def sparse_mla_decode(q, kv, indices, sm_scale, topk=None, topk_length=None, att
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _check(lib.sparse_mla_decode(ctypes.byref(a), int(num_splits), workspace.data_ptr(),
                                  workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+    return out, lse
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def sparse_mla_decode_noalloc(q, kv, indices, sm_scale, topk=None, topk_length=None, attn_sink=None,
+                              block_table=None, tokens_per_req=1, num_splits=0, out=None, lse=None,
+                              stream=None):
+    """Split-K decode whose partials live in the library's built-in scratch
+    array: for callers that cannot allocate device memory.  ``out``/``lse``
+    must be passed to allocate nothing here either."""
+    lib = load()
+    topk = indices.shape[1] if topk is None else topk
+    out, lse = _outputs(q, out, lse)
+    a = make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length, attn_sink, block_table,
+                  tokens_per_req)
+    _check(lib.sparse_mla_decode_noalloc(ctypes.byref(a), int(num_splits), _stream_handle(stream)))
     return out, lse
 
 

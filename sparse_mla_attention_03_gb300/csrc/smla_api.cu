@@ -249,3 +249,19 @@ int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags) {
 }
 
 }  // extern "C"
+
+// Accessors for other translation units of the library (same behaviour as the
+// helpers above; nothing here changes the entry points defined in this file).
+namespace smla {
+namespace host {
+int validate_args(const smla_args* a) { return validate(a); }
+int setup_device(int* dev) { return device_setup(dev); }
+KParams params_for(const smla_args* a, int dev) { return make_params(a, dev); }
+int num_sms(int dev) { return g_num_sms[dev]; }
+int decode_splits(int T, int H, int topk, int num_splits, int sms) {
+  return splits_for(T, H, topk, num_splits, sms);
+}
+size_t decode_ws_bytes(int64_t T, int64_t H, int64_t S) { return ws_bytes(T, H, S); }
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace host
+}  // namespace smla
