@@ -181,6 +181,28 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
+# ------------------------------------------------------------------------------------------ ranks
+def rank_seed(seed, rank):
+    """Each rank draws its own batch of the workload (weak scaling: no shared data, no collective)."""
+    return seed + 1000003 * rank
+
+
+def global_elapsed_ms(local_ms, world, device=None):
+    """The job's time is the slowest rank's: max over ranks (a timing-only all-reduce)."""
+    if world <= 1:
+        return float(local_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank_step, steps, world, elapsed_ms):
+    """Whole-job query tokens per second: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank_step * steps * world / (elapsed_ms / 1e3)
+
+
 # ------------------------------------------------------------------------------------------ runs
 def make_call(kind, binding, d, wl, out, lse, ws, num_splits):
     if kind == "prefill":
@@ -209,7 +231,7 @@ def run_ours(args, rank, world, local_rank):
     peaks = load_peaks()
     parts = []
     for tag, mk in spec["parts"]:
-        wl = mk(args.seed + rank)
+        wl = mk(rank_seed(args.seed, rank))
         d = {k: (None if getattr(wl, k) is None else getattr(wl, k).to(dev))
              for k in ("q", "kv", "indices", "topk_length", "attn_sink", "block_table")}
         out = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, device=dev)
@@ -248,13 +270,9 @@ def run_ours(args, rank, world, local_rank):
         wall = time.perf_counter() - t0
     per_part_ms = [[ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps)] for j in range(len(parts))]
     step_ms = [sum(per_part_ms[j][s] for j in range(len(parts))) for s in range(args.steps)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = global_elapsed_ms(sum(step_ms), world, dev)
     tokens_per_step = sum(p["wl"].T for p in parts)
-    value = tokens_per_step * args.steps * world / (total_ms / 1e3)
+    value = job_throughput(tokens_per_step, args.steps, world, total_ms)
 
     # roofline of the dominant kernel (the attention kernel; for decode the split kernel dominates)
     flops = sum(p["work"]["flops"] for p in parts)
