@@ -127,7 +127,7 @@ int splits_for(int T, int H, int topk, int num_splits, int num_sms) {
   if (num_splits > 0) {
     S = num_splits < chunks ? num_splits : chunks;
   } else {
-    const int hpc = smla::mma_heads_per_cta(H);
+    const int hpc = smla::heads_per_cta(H);
     const int64_t base = (int64_t)T * ((H + hpc - 1) / hpc);
     const int64_t target = 2LL * (num_sms > 0 ? num_sms : 148);
     S = 1;
@@ -161,7 +161,7 @@ int sparse_mla_prefill(const smla_args* a, smla_stream_t stream) {
   int dev;
   if ((rc = device_setup(&dev)) != SMLA_OK) return rc;
   smla::KParams p = make_params(a, dev);
-  cudaError_t e = smla::launch_mma(p, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = smla::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   return SMLA_OK;
 }
@@ -207,7 +207,7 @@ int sparse_mla_decode(const smla_args* a, int32_t num_splits, void* workspace, s
   p.ws_o = static_cast<float*>(workspace);
   p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = smla::launch_mma(p, st);
+  cudaError_t e = smla::launch_attention(p, st);
   if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode split launch: %s", cudaGetErrorString(e));
   e = smla::launch_combine(p, st);
   if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode combine launch: %s", cudaGetErrorString(e));

@@ -91,7 +91,7 @@ extern "C" int sparse_mla_decode_noalloc(const smla_args* a, int32_t num_splits,
   p.ws_o = static_cast<float*>(scratch);
   p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) + ((o_bytes + 255) / 256) * 256);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = smla::launch_mma(p, st);
+  cudaError_t e = smla::launch_attention(p, st);
   if (e != cudaSuccess) return smla::host::set_error(SMLA_ERR_CUDA, cudaGetErrorString(e));
   e = smla::launch_combine(p, st);
   if (e != cudaSuccess) return smla::host::set_error(SMLA_ERR_CUDA, cudaGetErrorString(e));
