@@ -185,7 +185,10 @@ __device__ __forceinline__ int q_prescale_exp(float amax) {
   if (!(amax > 0.f) || !isfinite(amax)) return 0;
   int e;
   frexpf(amax, &e);  // amax = m * 2^e, m in [0.5, 1)
-  return e - 15;
+  e -= 15;
+  return e < -100 ? -100 : (e > 100 ? 100 : e);
 }
+// 2^e as a float, exact for |e| <= 126.
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
 
 }  // namespace smla

@@ -42,7 +42,9 @@ namespace tc_path {
 
 constexpr int BM = 128;  // candidate rows per tile (MMA M)
 constexpr int HG = 64;   // heads per CTA (MMA N)
-constexpr int NT = 288;
+constexpr int NT = 416;   // 8 producer warps, 4 softmax warps, 1 MMA warp
+constexpr int W_SOFT = 8;
+constexpr int W_MMA = 12;
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 
 // shared memory map (offsets from a 1024-aligned base)
@@ -54,12 +56,15 @@ constexpr int OFF_TMAX = OFF_QMUL + 256;          // float [4][64]
 constexpr int OFF_MREF = OFF_TMAX + 1024;         // float [64]
 constexpr int OFF_ALPHA = OFF_MREF + 256;         // float [64]
 constexpr int OFF_LSUM = OFF_ALPHA + 256;         // float [4][64]
-constexpr int OFF_MISC = OFF_LSUM + 1024;         // barriers, flags, tmem base
+constexpr int OFF_MNEG = OFF_LSUM + 1024;         // float [64]: -reference max (0 while unset)
+constexpr int OFF_SCALE = OFF_MNEG + 256;         // float [8 warps][16 rows][4]
+constexpr int OFF_MISC = OFF_SCALE + 2048;        // barriers, flags, tmem base
 constexpr int SMEM_USED = OFF_MISC + 256;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;      // + alignment slack
 
 // barrier slots in OFF_MISC (8 bytes each)
-enum { B_KV0 = 0, B_SFULL = 5, B_PFULL = 6, B_PV0 = 7, B_DRAIN = 11, B_QFULL = 12, N_BARS = 13 };
+enum { B_KV0 = 0, B_SFULL = 5, B_PFULL = 6, B_PV0 = 7, B_DRAIN = 11, B_QFULL = 12, B_QRAW = 13, B_QCONV = 14,
+       N_BARS = 15 };
 constexpr int OFF_FLAGS = OFF_MISC + N_BARS * 8;  // int abort, int rescale, uint32 tmem base
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -193,6 +198,112 @@ __device__ __forceinline__ uint32_t sw128(int r, int ch) {
 
 // Warp transpose-reduction of 64 per-lane values: lane l receives the
 // reduction over all 32 lanes of entries 2l and 2l+1.
+
+// Warp transpose-reduction of 32 per-lane values x[B .. B+32): lane l receives
+// the reduction over all 32 lanes of entry B + l.
+template <bool kMax, int B, int N>
+__device__ __forceinline__ float xreduce32_at(const float (&xa)[N]) {
+  const float* x = xa + B;
+  const int lane = threadIdx.x & 31;
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float b[16];
+  {
+    const bool hi = lane & 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float send = hi ? x[j] : x[16 + j];
+      const float keep = hi ? x[16 + j] : x[j];
+      b[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    }
+  }
+  float c[8];
+  {
+    const bool hi = lane & 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float send = hi ? b[j] : b[8 + j];
+      const float keep = hi ? b[8 + j] : b[j];
+      c[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    }
+  }
+  float d[4];
+  {
+    const bool hi = lane & 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float send = hi ? c[j] : c[4 + j];
+      const float keep = hi ? c[4 + j] : c[j];
+      d[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    }
+  }
+  float e[2];
+  {
+    const bool hi = lane & 2;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float send = hi ? d[j] : d[2 + j];
+      const float keep = hi ? d[2 + j] : d[j];
+      e[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    }
+  }
+  const bool hi = lane & 1;
+  const float send = hi ? e[0] : e[1];
+  const float keep = hi ? e[1] : e[0];
+  return op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+}
+
+// Warp transpose-reduction of 32 per-lane values: lane l receives the
+// reduction over all 32 lanes of entry l.
+template <bool kMax>
+__device__ __forceinline__ float xreduce32(const float (&x)[32]) {
+  const int lane = threadIdx.x & 31;
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float b[16];
+  {
+    const bool hi = lane & 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float send = hi ? x[j] : x[16 + j];
+      const float keep = hi ? x[16 + j] : x[j];
+      b[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    }
+  }
+  float c[8];
+  {
+    const bool hi = lane & 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float send = hi ? b[j] : b[8 + j];
+      const float keep = hi ? b[8 + j] : b[j];
+      c[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    }
+  }
+  float d[4];
+  {
+    const bool hi = lane & 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float send = hi ? c[j] : c[4 + j];
+      const float keep = hi ? c[4 + j] : c[j];
+      d[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    }
+  }
+  float e[2];
+  {
+    const bool hi = lane & 2;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float send = hi ? d[j] : d[2 + j];
+      const float keep = hi ? d[2 + j] : d[j];
+      e[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    }
+  }
+  const bool hi = lane & 1;
+  const float send = hi ? e[0] : e[1];
+  const float keep = hi ? e[1] : e[0];
+  return op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+}
+
 template <bool kMax>
 __device__ __forceinline__ void xreduce64(const float (&x)[64], float& r0, float& r1) {
   const int lane = threadIdx.x & 31;
@@ -246,6 +357,109 @@ __device__ __forceinline__ void xreduce64(const float (&x)[64], float& r0, float
   }
 }
 
+// Producer warp pw (0..7) owns tile rows 16pw .. 16pw+15.  Its loads are
+// coalesced: one warp instruction reads 128 contiguous bytes (one 128-dim
+// group) of 4 rows (lanes 8j'..8j'+7 -> row 4j + j'), and the 16 rows' scale and
+// rope chunks (9 per row) are read as 144 consecutive (row, chunk) pairs.  All
+// 21 loads per lane are issued as soon as the previous tile is stored, before
+// waiting for the previous PV.
+__device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32_t sbase, uint32_t bars, int t,
+                                         int lo, int hi, int ntiles, int pw, int lane, volatile int* s_abort) {
+  const int32_t* idx_row = p.indices + (int64_t)t * p.idx_stride_t;
+  const int32_t* btr = bt_row_of(p, t);
+  float* s_sc = reinterpret_cast<float*>(smem + OFF_SCALE) + pw * 64;  // [16 rows][4]
+  uint4 nope[4][4];  // [group][j]: row 4j + lane/8, chunk 8g + lane%8
+  uint4 tail[5];     // flat (row, chunk) f = 32k + lane: row f/9, chunk 32 + f%9
+  auto issue = [&](int it) {
+    int rowid = -1;
+    if (lane < 16) {
+      const int slot = lo + it * BM + 16 * pw + lane;
+      if (slot < hi) rowid = resolve_row(p, btr, __ldg(idx_row + slot));
+    }
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = __shfl_sync(0xffffffffu, rowid, 4 * j + (lane >> 3));
+      const uint4* src = reinterpret_cast<const uint4*>(p.kv + (int64_t)(r < 0 ? 0 : r) * kRowBytes);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) nope[g][j] = r >= 0 ? __ldg(src + 8 * g + (lane & 7)) : z;
+    }
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+      const int f = 32 * k + lane;
+      const int rr = f < 144 ? f / 9 : 0;
+      const int r = __shfl_sync(0xffffffffu, rowid, rr);
+      const uint4* src = reinterpret_cast<const uint4*>(p.kv + (int64_t)(r < 0 ? 0 : r) * kRowBytes);
+      tail[k] = (f < 144 && r >= 0) ? __ldg(src + 32 + (f - 9 * rr)) : z;
+    }
+  };
+  if (ntiles > 0) issue(0);
+  // the tile buffer holds the raw q until the softmax warps have converted it
+  if (ntiles > 0 && !mbar_wait(bars + 8u * B_QCONV, 0, s_abort, p.err)) return;
+  for (int it = 0; it < ntiles; ++it) {
+    // scales of the 16 rows (invalid rows have zero data and zero scale)
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+      const int f = 32 * k + lane;
+      if (f < 144 && f % 9 == 0) {
+        const int rr = f / 9;
+        s_sc[rr * 4 + 0] = __uint_as_float(tail[k].x);
+        s_sc[rr * 4 + 1] = __uint_as_float(tail[k].y);
+        s_sc[rr * 4 + 2] = __uint_as_float(tail[k].z);
+        s_sc[rr * 4 + 3] = __uint_as_float(tail[k].w);
+        if (!(__uint_as_float(tail[k].x) <= 128.f && __uint_as_float(tail[k].y) <= 128.f &&
+              __uint_as_float(tail[k].z) <= 128.f && __uint_as_float(tail[k].w) <= 128.f))
+          atomicOr(p.err, kErrScaleRange);
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int g = 0; g < 5; ++g) {
+      // this region of the tile is free once the previous tile's PV used it
+      if (it > 0 && !mbar_wait(bars + 8u * (B_PV0 + (g < 4 ? g : 3)), (it - 1) & 1, s_abort, p.err)) return;
+      if (g < 4) {
+        const int c = 8 * g + (lane & 7);  // nope chunk: dims 16c .. 16c+15
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int rl = 4 * j + (lane >> 3);
+          const int row = 16 * pw + rl;
+          const __half2 sc2 = __float2half2_rn(s_sc[rl * 4 + g]);
+          const uint32_t sc2u = *reinterpret_cast<const uint32_t*>(&sc2);
+          const uint32_t w[4] = {nope[g][j].x, nope[g][j].y, nope[g][j].z, nope[g][j].w};
+          uint32_t h[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            e4m3x4_to_f16x2x2(w[i], h[2 * i], h[2 * i + 1]);
+            h[2 * i] = hmul2_u32(h[2 * i], sc2u);
+            h[2 * i + 1] = hmul2_u32(h[2 * i + 1], sc2u);
+          }
+          const uint32_t base = sbase + OFF_TILE + (c >> 2) * 16384;
+          const int oc = 2 * (c & 3);
+          // lanes 4..7 of each group of 8 store their odd chunk first, so the 8
+          // lanes of a store phase hit 8 distinct 16-byte bank groups
+          const bool sw = (lane & 4) != 0;
+          sts128(base + sw128(row, oc + (sw ? 1 : 0)),
+                 sw ? make_uint4(h[4], h[5], h[6], h[7]) : make_uint4(h[0], h[1], h[2], h[3]));
+          sts128(base + sw128(row, oc + (sw ? 0 : 1)),
+                 sw ? make_uint4(h[0], h[1], h[2], h[3]) : make_uint4(h[4], h[5], h[6], h[7]));
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 5; ++k) {
+          const int f = 32 * k + lane;
+          if (f < 144 && f % 9 != 0) {
+            const int rr = f / 9;
+            sts128(sbase + OFF_ROPE + sw128(16 * pw + rr, f - 9 * rr - 1), tail[k]);
+          }
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive(bars + 8u * (B_KV0 + g));
+    }
+    if (it + 1 < ntiles) issue(it + 1);
+  }
+}
+
 __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -269,24 +483,43 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   float* s_mref = reinterpret_cast<float*>(smem + OFF_MREF);
   float* s_alpha = reinterpret_cast<float*>(smem + OFF_ALPHA);
   float* s_lsum = reinterpret_cast<float*>(smem + OFF_LSUM);
+  float* s_mneg = reinterpret_cast<float*>(smem + OFF_MNEG);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_FLAGS);
-  volatile int* s_rescale = reinterpret_cast<volatile int*>(smem + OFF_FLAGS + 4);
+  volatile int* s_flag = reinterpret_cast<volatile int*>(smem + OFF_FLAGS + 4);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_FLAGS + 8);
   const uint32_t bars = sbase + OFF_MISC;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
   // ---------------------------------------------------------------- setup
-  if (warp == 8) {
+  if (warp == W_MMA) {
     if (lane == 0) {
-      for (int g = 0; g < 5; ++g) mbar_init(bar(B_KV0 + g), 128);
+      for (int g = 0; g < 5; ++g) mbar_init(bar(B_KV0 + g), 256);
       mbar_init(bar(B_SFULL), 1);
       mbar_init(bar(B_PFULL), 128);
       for (int c = 0; c < 4; ++c) mbar_init(bar(B_PV0 + c), 1);
       mbar_init(bar(B_DRAIN), 1);
       mbar_init(bar(B_QFULL), 128);
+      mbar_init(bar(B_QRAW), 1);
+      mbar_init(bar(B_QCONV), 128);
       *s_abort = 0;
-      *s_rescale = 0;
+      *s_flag = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      // raw q rows of this token's head group (64 x 1152 contiguous bytes) ->
+      // the tile buffer, with one bulk copy per 8 KB
+      const __nv_bfloat16* qsrc = p.q + (int64_t)t * p.q_stride_t + (int64_t)h0 * kDQK;
+      const bool bulk = (reinterpret_cast<uintptr_t>(qsrc) & 15) == 0;
+      *(volatile int*)(smem + OFF_FLAGS + 12) = bulk ? 1 : 0;
+      if (bulk) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar(B_QRAW)), "r"(HG * kDQK * 2)
+                     : "memory");
+#pragma unroll 1
+        for (int k = 0; k < 9; ++k)
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 8192, [%2];" ::"r"(
+                  sbase + OFF_TILE + k * 8192),
+              "l"(reinterpret_cast<const uint8_t*>(qsrc) + k * 8192), "r"(bar(B_QRAW))
+              : "memory");
+      }
     }
     __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(s_tmem))
@@ -300,120 +533,48 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   const uint32_t T_S = tmem;        // S^T: cols [0, 64)
   const uint32_t T_O = tmem + 64;   // O^T chunk c: cols [64 + 64c, 128 + 64c)
 
-  if (warp < 4) {
+  if (warp < W_SOFT) {
     // ============================================================ producers
-    const int pr = tid;  // row of the tile
-    const int32_t* idx_row = p.indices + (int64_t)t * p.idx_stride_t;
-    const int32_t* btr = bt_row_of(p, t);
-    for (int it = 0; it < ntiles; ++it) {
-      const int slot = lo + it * BM + pr;
-      const int row = slot < hi ? resolve_row(p, btr, __ldg(idx_row + slot)) : -1;
-      const uint4* src = reinterpret_cast<const uint4*>(p.kv + (int64_t)(row < 0 ? 0 : row) * kRowBytes);
-      const bool ok = row >= 0;
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      const uint4 scv = ok ? __ldg(src + 32) : z;
-      uint4 cur[8], nxt[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) cur[j] = ok ? __ldg(src + j) : z;
-      bool alive = true;
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        if (g < 3) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) nxt[j] = ok ? __ldg(src + 8 * (g + 1) + j) : z;
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) nxt[j] = ok ? __ldg(src + 33 + j) : z;  // rope
-        }
-        const float sc = __uint_as_float(g == 0 ? scv.x : (g == 1 ? scv.y : (g == 2 ? scv.z : scv.w)));
-        if (ok && !(sc <= 128.f)) atomicOr(p.err, kErrScaleRange);
-        const __half2 sc2 = __float2half2_rn(sc);
-        const uint32_t sc2u = *reinterpret_cast<const uint32_t*>(&sc2);
-        // the block pair 2g, 2g+1 of this tile is free once PV of the previous tile used chunk g
-        if (it > 0 && !mbar_wait(bar(B_PV0 + g), (it - 1) & 1, s_abort, p.err)) {
-          alive = false;
-          break;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          // 16 codes = dims 128g + 16j .. +15 -> two 16-byte f16 chunks
-          const uint32_t w[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
-          uint32_t h[8];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            e4m3x4_to_f16x2x2(w[k], h[2 * k], h[2 * k + 1]);
-            h[2 * k] = hmul2_u32(h[2 * k], sc2u);
-            h[2 * k + 1] = hmul2_u32(h[2 * k + 1], sc2u);
-          }
-          const int kb = 2 * g + (j >> 2);
-          const int oc = 2 * (j & 3);
-          const uint32_t base = sbase + OFF_TILE + kb * 16384;
-          sts128(base + sw128(pr, oc), make_uint4(h[0], h[1], h[2], h[3]));
-          sts128(base + sw128(pr, oc + 1), make_uint4(h[4], h[5], h[6], h[7]));
-        }
-        fence_proxy_async();
-        mbar_arrive(bar(B_KV0 + g));
-#pragma unroll
-        for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
-      }
-      if (!alive) break;
-      // rope: the region also holds P^T of the previous tile -> wait for its PV to finish
-      if (it > 0 && !mbar_wait(bar(B_PV0 + 3), (it - 1) & 1, s_abort, p.err)) break;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) sts128(sbase + OFF_ROPE + sw128(pr, j), cur[j]);
-      fence_proxy_async();
-      mbar_arrive(bar(B_KV0 + 4));
-    }
-  } else if (warp < 8) {
+    producer(p, smem, sbase, bars, t, lo, hi, ntiles, warp, lane, s_abort);
+  } else if (warp < W_MMA) {
     // ============================================================ softmax
     const int q4 = warp & 3;
     const int c = q4 * 32 + lane;  // TMEM lane: candidate (S^T) / dv row (O^T)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    // q of this token (while the producers gather the first tile): warp w
-    // converts heads 16(w-4) .. +15 in two rounds of 8; lane l owns head
-    // (l / 4) of the round and 16-byte chunks (l % 4) + 4k, k < 18.
-#pragma unroll 1
-    for (int round = 0; round < 2; ++round) {
-      const int hh = 16 * q4 + 8 * round + (lane >> 2);
-      const int sub = lane & 3;
-      const __nv_bfloat16* qrow = p.q + (int64_t)t * p.q_stride_t + (int64_t)(h0 + hh) * kDQK;
-      const bool vec = (reinterpret_cast<uintptr_t>(qrow) & 15) == 0;
-      uint4 v[18];
-#pragma unroll
-      for (int k = 0; k < 18; ++k) {
-        const int ch = sub + 4 * k;
-        if (vec) {
-          v[k] = __ldg(reinterpret_cast<const uint4*>(qrow) + ch);
-        } else {
-          uint16_t e[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) e[i] = __ldg(reinterpret_cast<const unsigned short*>(qrow) + ch * 8 + i);
-          v[k] = make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16),
-                            e[4] | ((uint32_t)e[5] << 16), e[6] | ((uint32_t)e[7] << 16));
-        }
+    // q of this token (while the producers gather the first tile).
+    const bool bulk = *(volatile int*)(smem + OFF_FLAGS + 12) != 0;
+    if (bulk) {
+      // raw bf16 q sits in the tile buffer: thread c handles head c/2, 16-byte
+      // chunks [36 (c%2), 36 (c%2) + 36) of its 72
+      const int hh = c >> 1, half = c & 1;
+      const uint8_t* raw = smem + OFF_TILE + hh * (kDQK * 2) + half * 36 * 16;
+      if (!mbar_wait(bar(B_QRAW), 0, s_abort, p.err)) {
+        // abort: the tile loop below sees the flag
       }
       float amax = 0.f;
-#pragma unroll
-      for (int k = 0; k < 18; ++k) {
-        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll 4
+      for (int k = 0; k < 36; ++k) {
+        const uint4 v = *reinterpret_cast<const uint4*>(raw + k * 16);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
-          amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] << 16)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] & 0xFFFF0000u)));
         }
       }
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       const int e = q_prescale_exp(amax);
-#pragma unroll
-      for (int k = 0; k < 18; ++k) {
-        const int ch = sub + 4 * k;  // 8 dims: 8ch .. 8ch+7
-        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+      const float down = pow2f(-e);
+#pragma unroll 4
+      for (int k = 0; k < 36; ++k) {
+        const int ch = 36 * half + k;  // 8 dims: 8ch .. 8ch+7
+        const uint4 v = *reinterpret_cast<const uint4*>(raw + k * 16);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float a = ldexpf(__uint_as_float(w[i] << 16), -e);
-          const float b = ldexpf(__uint_as_float(w[i] & 0xFFFF0000u), -e);
+          const float a = __uint_as_float(wv[i] << 16) * down;
+          const float b = __uint_as_float(wv[i] & 0xFFFF0000u) * down;
           if (ch < 64) {
             const __half2 hv = __floats2half2_rn(a, b);
             o[i] = *reinterpret_cast<const uint32_t*>(&hv);
@@ -426,17 +587,67 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
                                      : OFF_Q + 8 * 8192 + sw128(hh, ch - 64);
         sts128(sbase + off, make_uint4(o[0], o[1], o[2], o[3]));
       }
-      if (sub == 0) {
-        s_qmul[hh] = p.sm_scale * kLog2e * ldexpf(1.f, e);
+      if (half == 0) {
+        s_qmul[hh] = p.sm_scale * kLog2e * pow2f(e);
         s_mref[hh] = -INFINITY;
+        s_mneg[hh] = 0.f;
+      }
+    } else {
+      // q rows not 16-byte aligned: load through registers, warp q4 converts
+      // heads 16 q4 .. +15 in two rounds of 8 (lane l: head l/4, chunks l%4 + 4k)
+#pragma unroll 1
+      for (int round = 0; round < 2; ++round) {
+        const int hh = 16 * q4 + 8 * round + (lane >> 2);
+        const int sub = lane & 3;
+        const unsigned short* qrow = reinterpret_cast<const unsigned short*>(
+            p.q + (int64_t)t * p.q_stride_t + (int64_t)(h0 + hh) * kDQK);
+        float amax = 0.f;
+#pragma unroll 1
+        for (int k = 0; k < 18; ++k)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)__ldg(qrow + (sub + 4 * k) * 8 + i) << 16)));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int e = q_prescale_exp(amax);
+        const float down = pow2f(-e);
+#pragma unroll 1
+        for (int k = 0; k < 18; ++k) {
+          const int ch = sub + 4 * k;
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float a = __uint_as_float((uint32_t)__ldg(qrow + ch * 8 + 2 * i) << 16) * down;
+            const float b = __uint_as_float((uint32_t)__ldg(qrow + ch * 8 + 2 * i + 1) << 16) * down;
+            if (ch < 64) {
+              const __half2 hv = __floats2half2_rn(a, b);
+              o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+            } else {
+              const __nv_bfloat162 bv = __floats2bfloat162_rn(a, b);
+              o[i] = *reinterpret_cast<const uint32_t*>(&bv);
+            }
+          }
+          const uint32_t off = ch < 64 ? OFF_Q + (ch >> 3) * 8192 + sw128(hh, ch & 7)
+                                       : OFF_Q + 8 * 8192 + sw128(hh, ch - 64);
+          sts128(sbase + off, make_uint4(o[0], o[1], o[2], o[3]));
+        }
+        if (sub == 0) {
+          s_qmul[hh] = p.sm_scale * kLog2e * pow2f(e);
+          s_mref[hh] = -INFINITY;
+          s_mneg[hh] = 0.f;
+        }
       }
     }
     fence_proxy_async();
     mbar_arrive(bar(B_QFULL));
+    mbar_arrive(bar(B_QCONV));  // the tile buffer is free for the producers
     named_bar(1, 128);  // s_qmul / s_mref visible to the other softmax warps
 
+    // running sums of P per head: lane l keeps heads l and l+32 of this warp's
+    // 32 candidates (summed over the warp by a transpose-reduction per tile)
     float lsum0 = 0.f, lsum1 = 0.f;
     bool alive = true;
+    bool refs_set = false;  // uniform: every head has a finite reference max
     const int32_t* idx_row = p.indices + (int64_t)t * p.idx_stride_t;
     const int32_t* btr = bt_row_of(p, t);
     for (int it = 0; it < ntiles; ++it) {
@@ -449,91 +660,114 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       }
       tc_fence_after();
       float x[64];
-      tmem_ld64(T_S + lane_off, x);
+      tmem_ld64(T_S + lane_off, x);  // one TMEM round trip per tile
+      // x = score (log2 units) minus the head's reference max
+      float dmax = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] * s_qmul[h] : -INFINITY;
-      float m0, m1;
-      xreduce64<true>(x, m0, m1);
-      s_tmax[q4 * 64 + 2 * lane] = m0;
-      s_tmax[q4 * 64 + 2 * lane + 1] = m1;
-      named_bar(1, 128);
-      if (q4 == 0) {
-        bool need = false;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int h = 2 * lane + j;
-          const float tm = fmaxf(fmaxf(s_tmax[h], s_tmax[64 + h]), fmaxf(s_tmax[128 + h], s_tmax[192 + h]));
-          const float mo = s_mref[h];
-          float al = 1.f;
-          if (tm > mo + 8.f) {  // also when mo == -inf and tm is finite
-            al = exp2f(mo - tm);
-            s_mref[h] = tm;
-            need = true;
-          }
-          s_alpha[h] = al;
-        }
-        need = __any_sync(0xffffffffu, need);
-        if (lane == 0) *s_rescale = need ? 1 : 0;
+      for (int h4 = 0; h4 < 16; ++h4) {
+        const float4 qm = *reinterpret_cast<const float4*>(s_qmul + 4 * h4);
+        const float4 mn = *reinterpret_cast<const float4*>(s_mneg + 4 * h4);
+        x[4 * h4 + 0] = fmaf(x[4 * h4 + 0], qm.x, mn.x);
+        x[4 * h4 + 1] = fmaf(x[4 * h4 + 1], qm.y, mn.y);
+        x[4 * h4 + 2] = fmaf(x[4 * h4 + 2], qm.z, mn.z);
+        x[4 * h4 + 3] = fmaf(x[4 * h4 + 3], qm.w, mn.w);
+        dmax = fmaxf(dmax, fmaxf(fmaxf(x[4 * h4], x[4 * h4 + 1]), fmaxf(x[4 * h4 + 2], x[4 * h4 + 3])));
       }
-      named_bar(1, 128);
-      const bool rescale = *s_rescale != 0;
-      // P = exp2(x - mref) rounded to f16, row c of P^T (MN-major: heads contiguous)
-      float pf[64];
+      if (!valid) dmax = -INFINITY;
+      // Slow path (first tile with data, or a score 2^8 above its reference):
+      // exact per-head tile maxima, raise the references, rescale sums and O^T.
+      if (bar_or(1, 128, (!refs_set && valid) || dmax > 8.f)) {
+#pragma unroll
+        for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] - s_mneg[h] : -INFINITY;  // raw scores
+        s_tmax[q4 * 64 + lane] = xreduce32_at<true, 0>(x);
+        s_tmax[q4 * 64 + 32 + lane] = xreduce32_at<true, 32>(x);
+        named_bar(1, 128);
+        if (q4 == 0) {
+          bool any_set = true;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int h = lane + 32 * j;
+            const float tm = fmaxf(fmaxf(s_tmax[h], s_tmax[64 + h]), fmaxf(s_tmax[128 + h], s_tmax[192 + h]));
+            const float mo = s_mref[h];
+            float al = 1.f;
+            if (tm > mo + 8.f || (mo == -INFINITY && tm > -INFINITY)) {
+              al = mo == -INFINITY ? 0.f : exp2f(mo - tm);
+              s_mref[h] = tm;
+              s_mneg[h] = -tm;
+            }
+            any_set = any_set && (s_mref[h] > -INFINITY);
+            s_alpha[h] = al;
+          }
+          any_set = __all_sync(0xffffffffu, any_set);
+          if (lane == 0) *s_flag = any_set ? 1 : 0;
+        }
+        named_bar(1, 128);
+        refs_set = *s_flag != 0;
+        lsum0 *= s_alpha[lane];
+        lsum1 *= s_alpha[lane + 32];
+        if (it > 0) {
+          // O^T columns of rescaled heads (the previous PV has completed: S^T of
+          // this tile was issued after it and has been waited for)
+#pragma unroll 1
+          for (int part = 0; part < 16; ++part) {
+            const int col = 16 * part, hb = col & 63;
+            float o[16];
+            tmem_ld16(T_O + col + lane_off, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 16; ++h) o[h] *= s_alpha[hb + h];
+            tmem_st16(T_O + col + lane_off, o);
+          }
+          tmem_st_wait();
+        }
+        // scores again from TMEM, against the new references
+        tmem_ld64(T_S + lane_off, x);
+#pragma unroll
+        for (int h4 = 0; h4 < 16; ++h4) {
+          const float4 qm = *reinterpret_cast<const float4*>(s_qmul + 4 * h4);
+          const float4 mn = *reinterpret_cast<const float4*>(s_mneg + 4 * h4);
+          x[4 * h4 + 0] = fmaf(x[4 * h4 + 0], qm.x, mn.x);
+          x[4 * h4 + 1] = fmaf(x[4 * h4 + 1], qm.y, mn.y);
+          x[4 * h4 + 2] = fmaf(x[4 * h4 + 2], qm.z, mn.z);
+          x[4 * h4 + 3] = fmaf(x[4 * h4 + 3], qm.w, mn.w);
+        }
+      }
+      // P = exp2(x) rounded to f16 -> row c of P^T (MN-major: heads contiguous)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         uint32_t pk[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int h = 8 * j + 2 * k;
-          const float r0 = s_mref[h], r1 = s_mref[h + 1];
-          const float e0 = exp2f(x[h] - (r0 == -INFINITY ? 0.f : r0));
-          const float e1 = exp2f(x[h + 1] - (r1 == -INFINITY ? 0.f : r1));
+          const float e0 = valid ? exp2f(x[h]) : 0.f;
+          const float e1 = valid ? exp2f(x[h + 1]) : 0.f;
+          x[h] = e0;
+          x[h + 1] = e1;
           const __half2 hv = __floats2half2_rn(e0, e1);
           pk[k] = *reinterpret_cast<const uint32_t*>(&hv);
-          const float2 back = __half22float2(hv);
-          pf[h] = back.x;
-          pf[h + 1] = back.y;
         }
         sts128(sbase + OFF_ROPE + sw128(c, j), make_uint4(pk[0], pk[1], pk[2], pk[3]));
-      }
-      float t0, t1;
-      xreduce64<false>(pf, t0, t1);
-      lsum0 = fmaf(lsum0, s_alpha[2 * lane], t0);
-      lsum1 = fmaf(lsum1, s_alpha[2 * lane + 1], t1);
-      if (rescale && it > 0) {
-        // O^T columns of rescaled heads (the previous PV has completed: S^T of
-        // this tile was issued after it and has been waited for)
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          float o[64];
-          tmem_ld64(T_O + 64 * ch + lane_off, o);
-#pragma unroll
-          for (int h = 0; h < 64; ++h) o[h] *= s_alpha[h];
-          tmem_st16(T_O + 64 * ch + lane_off, o);
-          tmem_st16(T_O + 64 * ch + 16 + lane_off, o + 16);
-          tmem_st16(T_O + 64 * ch + 32 + lane_off, o + 32);
-          tmem_st16(T_O + 64 * ch + 48 + lane_off, o + 48);
-        }
-        tmem_st_wait();
       }
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL));
+      lsum0 += xreduce32_at<false, 0>(x);
+      lsum1 += xreduce32_at<false, 32>(x);
     }
     // ---------------------------------------------------------- epilogue
     bool failed = !alive;
     if (alive && ntiles > 0 && !mbar_wait(bar(B_PV0 + 3), (ntiles - 1) & 1, s_abort, p.err)) failed = true;
-    s_lsum[q4 * 64 + 2 * lane] = lsum0;
-    s_lsum[q4 * 64 + 2 * lane + 1] = lsum1;
+    s_lsum[q4 * 64 + lane] = lsum0;
+    s_lsum[q4 * 64 + 32 + lane] = lsum1;
     alive = !bar_or(1, 128, failed);
     if (alive) {
       tc_fence_after();
       const bool final_out = p.ws_o == nullptr;
-      // per-head normaliser and lse (lane handles heads 2l, 2l+1 in warp 4)
+      // per-head normaliser and lse (warp 8: lane handles heads l and l+32)
       if (q4 == 0) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const int hh = 2 * lane + j;
+          const int hh = lane + 32 * j;
           const int h = h0 + hh;
           const float lt = s_lsum[hh] + s_lsum[64 + hh] + s_lsum[128 + hh] + s_lsum[192 + hh];
           const float m = s_mref[hh];
@@ -553,9 +787,11 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
         }
       }
       named_bar(1, 128);
-      // stage [64 heads x 512 dv] in the (now idle) tile buffer, then store rows
+      // outputs straight from TMEM: per head, a warp's 32 lanes store 32
+      // consecutive d_v values (64 or 128 contiguous bytes)
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
+        const int dv = 128 * ch + c;
         float o[64];
         if (ntiles > 0) {
           tmem_ld64(T_O + 64 * ch + lane_off, o);
@@ -563,32 +799,14 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
 #pragma unroll
           for (int h = 0; h < 64; ++h) o[h] = 0.f;
         }
-        const int dv = 128 * ch + c;
         if (final_out) {
-          __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(smem + OFF_TILE);
+          __nv_bfloat16* ob = p.out + (int64_t)t * p.out_stride_t + (int64_t)h0 * kDV + dv;
 #pragma unroll
-          for (int h = 0; h < 64; ++h) st[h * kDV + dv] = __float2bfloat16_rn(o[h] * s_alpha[h]);
+          for (int h = 0; h < 64; ++h) ob[(int64_t)h * kDV] = __float2bfloat16_rn(o[h] * s_alpha[h]);
         } else {
-          float* st = reinterpret_cast<float*>(smem + OFF_TILE);
+          float* wb = p.ws_o + (((int64_t)t * p.H + h0) * p.num_splits + split) * kDV + dv;
 #pragma unroll
-          for (int h = 0; h < 64; ++h) st[h * kDV + dv] = o[h] * s_alpha[h];
-        }
-      }
-      named_bar(1, 128);
-      const int tl = tid - 128;
-      if (final_out) {
-        for (int i = tl; i < 64 * 128; i += 128) {  // 64 rows x 128 x 8 B
-          const int hh = i >> 7, part = i & 127;
-          const uint2 v = *reinterpret_cast<const uint2*>(smem + OFF_TILE + hh * 1024 + part * 8);
-          __nv_bfloat16* orow = p.out + (int64_t)t * p.out_stride_t + (int64_t)(h0 + hh) * kDV;
-          *reinterpret_cast<uint2*>(orow + part * 4) = v;
-        }
-      } else {
-        for (int i = tl; i < 64 * 128; i += 128) {  // 64 rows x 128 x 16 B
-          const int hh = i >> 7, part = i & 127;
-          const uint4 v = *reinterpret_cast<const uint4*>(smem + OFF_TILE + hh * 2048 + part * 16);
-          float* wrow = p.ws_o + (((int64_t)t * p.H + h0 + hh) * p.num_splits + split) * kDV;
-          *reinterpret_cast<uint4*>(wrow + part * 4) = v;
+          for (int h = 0; h < 64; ++h) wb[(int64_t)h * p.num_splits * kDV] = o[h] * s_alpha[h];
         }
       }
     }
@@ -644,10 +862,10 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       }
     }
   }
-  if (warp == 8) __syncwarp();
+  if (warp == W_MMA) __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == W_MMA) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
   }
