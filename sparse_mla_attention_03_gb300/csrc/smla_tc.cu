@@ -20,16 +20,19 @@
 //          reused for P^T [128 cand x 64 h] f16 once S^T is done.
 //   q       72 KB: q of the token, nope f16 / rope bf16, B operand of S^T.
 //
-// Warp roles (288 threads):
-//   warps 0-3  producers: thread p gathers row p of the tile straight from
-//              global memory, converts e4m3 -> f16 times its scale (exact while
-//              |value| <= 65504) and stores it swizzled; the bf16 rope is copied.
-//   warps 4-7  softmax/epilogue: thread = TMEM lane.  Per tile it reads its
-//              candidate's 64 scores, forms per-head tile maxima and sums with a
-//              warp transpose-reduction, keeps a per-head reference max that is
-//              only raised when a score exceeds it by 2^8 (then O^T columns and
-//              the sums are rescaled), and writes P (f16) for the PV MMA.
-//   warp 8     allocates TMEM; lane 0 issues every MMA and commit.
+// Warp roles (384 threads, so that each thread may hold 168 registers):
+//   warps 0-7   producers: warp w gathers rows 16w..16w+15 of each tile with
+//               coalesced 16-byte loads, converts e4m3 -> f16 times the row's
+//               scale (exact while |value| <= 65504) and stores it swizzled; the
+//               bf16 rope is copied as is.  The loads of tile i+1 are issued as
+//               soon as tile i is stored.
+//   warps 8-11  softmax/epilogue: thread = TMEM lane.  Per tile it reads its
+//               candidate's 64 scores once, keeps a per-head reference max that
+//               is only raised when a score exceeds it by 2^8 (then O^T columns
+//               and the sums are rescaled), writes P (f16) for the PV MMA and
+//               adds P into per-head sums with warp transpose-reductions.
+//               Lane 0 of warp 8 also allocates TMEM and issues every MMA:
+//               S^T of a tile before that tile's softmax, PV after it.
 //
 // Every mbarrier wait is bounded (about one second of global time); on timeout
 // the CTA sets the error word, stops, drains its issued MMAs, frees TMEM and
@@ -42,9 +45,8 @@ namespace tc_path {
 
 constexpr int BM = 128;  // candidate rows per tile (MMA M)
 constexpr int HG = 64;   // heads per CTA (MMA N)
-constexpr int NT = 416;   // 8 producer warps, 4 softmax warps, 1 MMA warp
+constexpr int NT = 384;   // 8 producer warps, 4 softmax warps
 constexpr int W_SOFT = 8;
-constexpr int W_MMA = 12;
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 
 // shared memory map (offsets from a 1024-aligned base)
@@ -63,8 +65,7 @@ constexpr int SMEM_USED = OFF_MISC + 256;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;      // + alignment slack
 
 // barrier slots in OFF_MISC (8 bytes each)
-enum { B_KV0 = 0, B_SFULL = 5, B_PFULL = 6, B_PV0 = 7, B_DRAIN = 11, B_QFULL = 12, B_QRAW = 13, B_QCONV = 14,
-       N_BARS = 15 };
+enum { B_KV0 = 0, B_SFULL = 5, B_PFULL = 6, B_PV0 = 7, B_DRAIN = 11, B_QRAW = 12, B_QCONV = 13, N_BARS = 14 };
 constexpr int OFF_FLAGS = OFF_MISC + N_BARS * 8;  // int abort, int rescale, uint32 tmem base
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -358,31 +359,41 @@ __device__ __forceinline__ void xreduce64(const float (&x)[64], float& r0, float
 }
 
 // Producer warp pw (0..7) owns tile rows 16pw .. 16pw+15.  Its loads are
-// coalesced: one warp instruction reads 128 contiguous bytes (one 128-dim
-// group) of 4 rows (lanes 8j'..8j'+7 -> row 4j + j'), and the 16 rows' scale and
-// rope chunks (9 per row) are read as 144 consecutive (row, chunk) pairs.  All
-// 21 loads per lane are issued as soon as the previous tile is stored, before
-// waiting for the previous PV.
+// coalesced (4 lanes read 64 contiguous bytes of one row), and the 16 rows'
+// scale and rope chunks (9 per row) are read as 144 consecutive (row, chunk)
+// pairs.  All 21 loads per lane are issued as soon as the previous tile is
+// stored, before waiting for the previous PV.
 __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32_t sbase, uint32_t bars, int t,
                                          int lo, int hi, int ntiles, int pw, int lane, volatile int* s_abort) {
   const int32_t* idx_row = p.indices + (int64_t)t * p.idx_stride_t;
   const int32_t* btr = bt_row_of(p, t);
   float* s_sc = reinterpret_cast<float*>(smem + OFF_SCALE) + pw * 64;  // [16 rows][4]
-  uint4 nope[4][4];  // [group][j]: row 4j + lane/8, chunk 8g + lane%8
+  // nope[g][j]: lane l holds row 8(j/2) + 2(l/8) + (l/4)%2, chunk 8g + 4(j%2) + l%4.
+  // Each 8-lane store phase then covers two adjacent rows, whose different
+  // swizzles put its 8 chunks in 8 distinct bank groups.
+  uint4 nope[4][4];
   uint4 tail[5];     // flat (row, chunk) f = 32k + lane: row f/9, chunk 32 + f%9
+  // index reads run one tile ahead of the row loads (lanes 0..15: one row each)
+  auto load_idx = [&](int it) -> int {
+    const int slot = lo + it * BM + 16 * pw + lane;
+    return (lane < 16 && it < ntiles && slot < hi) ? __ldg(idx_row + slot) : -1;
+  };
+  int idx_next = load_idx(0);
   auto issue = [&](int it) {
     int rowid = -1;
+    const int idx = idx_next;
+    idx_next = load_idx(it + 1);
     if (lane < 16) {
       const int slot = lo + it * BM + 16 * pw + lane;
-      if (slot < hi) rowid = resolve_row(p, btr, __ldg(idx_row + slot));
+      if (slot < hi) rowid = resolve_row(p, btr, idx);
     }
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int r = __shfl_sync(0xffffffffu, rowid, 4 * j + (lane >> 3));
+      const int r = __shfl_sync(0xffffffffu, rowid, 8 * (j >> 1) + 2 * (lane >> 3) + ((lane >> 2) & 1));
       const uint4* src = reinterpret_cast<const uint4*>(p.kv + (int64_t)(r < 0 ? 0 : r) * kRowBytes);
 #pragma unroll
-      for (int g = 0; g < 4; ++g) nope[g][j] = r >= 0 ? __ldg(src + 8 * g + (lane & 7)) : z;
+      for (int g = 0; g < 4; ++g) nope[g][j] = r >= 0 ? __ldg(src + 8 * g + 4 * (j & 1) + (lane & 3)) : z;
     }
 #pragma unroll
     for (int k = 0; k < 5; ++k) {
@@ -418,30 +429,28 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
       // this region of the tile is free once the previous tile's PV used it
       if (it > 0 && !mbar_wait(bars + 8u * (B_PV0 + (g < 4 ? g : 3)), (it - 1) & 1, s_abort, p.err)) return;
       if (g < 4) {
-        const int c = 8 * g + (lane & 7);  // nope chunk: dims 16c .. 16c+15
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int rl = 4 * j + (lane >> 3);
+          const int rl = 8 * (j >> 1) + 2 * (lane >> 3) + ((lane >> 2) & 1);
           const int row = 16 * pw + rl;
+          const int c = 8 * g + 4 * (j & 1) + (lane & 3);  // nope chunk: dims 16c .. 16c+15
           const __half2 sc2 = __float2half2_rn(s_sc[rl * 4 + g]);
           const uint32_t sc2u = *reinterpret_cast<const uint32_t*>(&sc2);
           const uint32_t w[4] = {nope[g][j].x, nope[g][j].y, nope[g][j].z, nope[g][j].w};
           uint32_t h[8];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            e4m3x4_to_f16x2x2(w[i], h[2 * i], h[2 * i + 1]);
+            asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n"
+                " cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+                : "=r"(h[2 * i]), "=r"(h[2 * i + 1])
+                : "r"(w[i]));
             h[2 * i] = hmul2_u32(h[2 * i], sc2u);
             h[2 * i + 1] = hmul2_u32(h[2 * i + 1], sc2u);
           }
           const uint32_t base = sbase + OFF_TILE + (c >> 2) * 16384;
           const int oc = 2 * (c & 3);
-          // lanes 4..7 of each group of 8 store their odd chunk first, so the 8
-          // lanes of a store phase hit 8 distinct 16-byte bank groups
-          const bool sw = (lane & 4) != 0;
-          sts128(base + sw128(row, oc + (sw ? 1 : 0)),
-                 sw ? make_uint4(h[4], h[5], h[6], h[7]) : make_uint4(h[0], h[1], h[2], h[3]));
-          sts128(base + sw128(row, oc + (sw ? 0 : 1)),
-                 sw ? make_uint4(h[0], h[1], h[2], h[3]) : make_uint4(h[4], h[5], h[6], h[7]));
+          sts128(base + sw128(row, oc), make_uint4(h[0], h[1], h[2], h[3]));
+          sts128(base + sw128(row, oc + 1), make_uint4(h[4], h[5], h[6], h[7]));
         }
       } else {
 #pragma unroll
@@ -491,14 +500,13 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
   // ---------------------------------------------------------------- setup
-  if (warp == W_MMA) {
+  if (warp == W_SOFT) {
     if (lane == 0) {
       for (int g = 0; g < 5; ++g) mbar_init(bar(B_KV0 + g), 256);
       mbar_init(bar(B_SFULL), 1);
       mbar_init(bar(B_PFULL), 128);
       for (int c = 0; c < 4; ++c) mbar_init(bar(B_PV0 + c), 1);
       mbar_init(bar(B_DRAIN), 1);
-      mbar_init(bar(B_QFULL), 128);
       mbar_init(bar(B_QRAW), 1);
       mbar_init(bar(B_QCONV), 128);
       *s_abort = 0;
@@ -536,9 +544,48 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   if (warp < W_SOFT) {
     // ============================================================ producers
     producer(p, smem, sbase, bars, t, lo, hi, ntiles, warp, lane, s_abort);
-  } else if (warp < W_MMA) {
-    // ============================================================ softmax
+  } else {
+    // ============================================================ softmax (+ MMA issue)
     const int q4 = warp & 3;
+    const bool issuer = warp == W_SOFT && lane == 0;
+    const uint32_t id_f16 = idesc(0, 0, 0);
+    const uint32_t id_bf16 = idesc(1, 0, 0);
+    const uint32_t id_pv = idesc(0, 1, 1);
+    const uint32_t a_tile = sbase + OFF_TILE, a_rope = sbase + OFF_ROPE, b_q = sbase + OFF_Q;
+    // S^T(it) = K_tile . Q^T, 128-dim group by group as the producers finish them
+    auto issue_st = [&](int it) {
+      for (int g = 0; g < 4; ++g) {
+        if (!mbar_wait(bar(B_KV0 + g), it & 1, s_abort, p.err)) return;
+        tc_fence_after();
+#pragma unroll
+        for (int kb2 = 0; kb2 < 2; ++kb2) {
+          const int kb = 2 * g + kb2;
+#pragma unroll
+          for (int st = 0; st < 4; ++st)
+            mma(T_S, sdesc(a_tile + kb * 16384 + st * 32, 16, 1024), sdesc(b_q + kb * 8192 + st * 32, 16, 1024),
+                id_f16, (kb | st) != 0);
+        }
+      }
+      if (!mbar_wait(bar(B_KV0 + 4), it & 1, s_abort, p.err)) return;
+      tc_fence_after();
+#pragma unroll
+      for (int st = 0; st < 4; ++st)
+        mma(T_S, sdesc(a_rope + st * 32, 16, 1024), sdesc(b_q + 8 * 8192 + st * 32, 16, 1024), id_bf16, 1);
+      mma_commit(bar(B_SFULL));
+    };
+    // O^T += V_tile^T . P^T, one commit per 128-row d_v chunk
+    auto issue_pv = [&](int it) {
+      if (!mbar_wait(bar(B_PFULL), it & 1, s_abort, p.err)) return;
+      tc_fence_after();
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma(T_O + 64 * ch, sdesc(a_tile + 2 * ch * 16384 + ks * 2048, 16384, 1024),
+              sdesc(a_rope + ks * 2048, 8192, 1024), id_pv, (it > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(bar(B_PV0 + ch));
+      }
+    };
     const int c = q4 * 32 + lane;  // TMEM lane: candidate (S^T) / dv row (O^T)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     // q of this token (while the producers gather the first tile).
@@ -639,9 +686,8 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       }
     }
     fence_proxy_async();
-    mbar_arrive(bar(B_QFULL));
     mbar_arrive(bar(B_QCONV));  // the tile buffer is free for the producers
-    named_bar(1, 128);  // s_qmul / s_mref visible to the other softmax warps
+    named_bar(1, 128);  // q, s_qmul and s_mref visible to all softmax warps and the issuer
 
     // running sums of P per head: lane l keeps heads l and l+32 of this warp's
     // 32 candidates (summed over the warp by a transpose-reduction per tile)
@@ -650,9 +696,21 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     bool refs_set = false;  // uniform: every head has a finite reference max
     const int32_t* idx_row = p.indices + (int64_t)t * p.idx_stride_t;
     const int32_t* btr = bt_row_of(p, t);
+    // the slot index of tile it+1 is read during tile it and resolved at its
+    // end, off the softmax's critical path
+    bool valid_next = false;
+    if (ntiles > 0 && lo + c < hi) valid_next = resolve_row(p, btr, __ldg(idx_row + lo + c)) >= 0;
+    int idx_ahead = (ntiles > 1 && lo + BM + c < hi) ? __ldg(idx_row + lo + BM + c) : -1;
     for (int it = 0; it < ntiles; ++it) {
       const int slot = lo + it * BM + c;
-      const bool valid = slot < hi && resolve_row(p, btr, __ldg(idx_row + slot)) >= 0;
+      const bool valid = valid_next;
+      const int idx1 = idx_ahead;
+      const int slot2 = slot + 2 * BM;
+      idx_ahead = (it + 2 < ntiles && slot2 < hi) ? __ldg(idx_row + slot2) : -1;
+      if (warp == W_SOFT) {
+        if (issuer) issue_st(it);
+        __syncwarp();
+      }
       const bool failed = !mbar_wait(bar(B_SFULL), it & 1, s_abort, p.err);
       if (bar_or(1, 128, failed)) {
         alive = false;
@@ -751,8 +809,13 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL));
+      if (warp == W_SOFT) {
+        if (issuer) issue_pv(it);
+        __syncwarp();
+      }
       lsum0 += xreduce32_at<false, 0>(x);
       lsum1 += xreduce32_at<false, 32>(x);
+      valid_next = (it + 1 < ntiles && slot + BM < hi) && resolve_row(p, btr, idx1) >= 0;
     }
     // ---------------------------------------------------------- epilogue
     bool failed = !alive;
@@ -810,62 +873,24 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
         }
       }
     }
-  } else if (lane == 0) {
-    // ============================================================ MMA issuer
-    const uint32_t id_f16 = idesc(0, 0, 0);
-    const uint32_t id_bf16 = idesc(1, 0, 0);
-    const uint32_t id_pv = idesc(0, 1, 1);
-    const uint32_t a_tile = sbase + OFF_TILE, a_rope = sbase + OFF_ROPE, b_q = sbase + OFF_Q;
-    const bool q_ok = mbar_wait(bar(B_QFULL), 0, s_abort, p.err);
-    for (int it = 0; it < (q_ok ? ntiles : 0); ++it) {
-      bool alive = true;
-      for (int g = 0; g < 4 && alive; ++g) {
-        if (!mbar_wait(bar(B_KV0 + g), it & 1, s_abort, p.err)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int kb2 = 0; kb2 < 2; ++kb2) {
-          const int kb = 2 * g + kb2;
-#pragma unroll
-          for (int s = 0; s < 4; ++s)
-            mma(T_S, sdesc(a_tile + kb * 16384 + s * 32, 16, 1024), sdesc(b_q + kb * 8192 + s * 32, 16, 1024),
-                id_f16, (kb | s) != 0);
+    if (warp == W_SOFT) {
+      if (issuer) {
+        // every issued MMA completes before TMEM is released
+        mma_commit(bar(B_DRAIN));
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(bar(B_DRAIN), 0)) {
+          if (globaltimer() - t0 > kTimeoutNs) {
+            atomicOr(p.err, kErrTimeout);
+            break;
+          }
         }
       }
-      if (!alive) break;
-      if (!mbar_wait(bar(B_KV0 + 4), it & 1, s_abort, p.err)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma(T_S, sdesc(a_rope + s * 32, 16, 1024), sdesc(b_q + 8 * 8192 + s * 32, 16, 1024), id_bf16, 1);
-      mma_commit(bar(B_SFULL));
-      if (!mbar_wait(bar(B_PFULL), it & 1, s_abort, p.err)) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma(T_O + 64 * ch, sdesc(a_tile + 2 * ch * 16384 + ks * 2048, 16384, 1024),
-              sdesc(a_rope + ks * 2048, 8192, 1024), id_pv, (it > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(bar(B_PV0 + ch));
-      }
-    }
-    // all issued MMAs complete before TMEM is released
-    mma_commit(bar(B_DRAIN));
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar(B_DRAIN), 0)) {
-      if (globaltimer() - t0 > kTimeoutNs) {
-        atomicOr(p.err, kErrTimeout);
-        break;
-      }
+      __syncwarp();
     }
   }
-  if (warp == W_MMA) __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == W_MMA) {
+  if (warp == W_SOFT) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
   }
