@@ -105,6 +105,18 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     }
   }
 }
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Warp-uniform bounded wait: every lane polls (a lane-0-only poll leaves the
+// warp diverged, and MMAs issued by a diverged warp run several times
+// slower), and the warp agrees on the verdict.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, err);
+  return __all_sync(0xffffffffu, ok);
+}
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -143,16 +155,19 @@ __host__ __device__ constexpr uint32_t idesc(uint32_t fmt, uint32_t a_major, uin
   return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_major << 15) | (b_major << 16) | ((uint32_t)(HG >> 3) << 17) |
          ((uint32_t)(BM >> 4) << 24);
 }
+// One MMA issued by one elected lane of a converged warp.
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
-          d_tmem),
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(id), "r"(acc)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
+      : "memory");
 }
 // 32 lanes x 16 consecutive 32-bit columns per thread.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
@@ -470,8 +485,10 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
 }
 
 __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base, by pointer arithmetic on the __shared__ array so
+  // that accesses through it stay shared-memory (not generic) accesses
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -547,7 +564,6 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   } else {
     // ============================================================ softmax (+ MMA issue)
     const int q4 = warp & 3;
-    const bool issuer = warp == W_SOFT && lane == 0;
     const uint32_t id_f16 = idesc(0, 0, 0);
     const uint32_t id_bf16 = idesc(1, 0, 0);
     const uint32_t id_pv = idesc(0, 1, 1);
@@ -555,7 +571,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     // S^T(it) = K_tile . Q^T, 128-dim group by group as the producers finish them
     auto issue_st = [&](int it) {
       for (int g = 0; g < 4; ++g) {
-        if (!mbar_wait(bar(B_KV0 + g), it & 1, s_abort, p.err)) return;
+        if (!mbar_wait_warp(bar(B_KV0 + g), it & 1, s_abort, p.err)) return;
         tc_fence_after();
 #pragma unroll
         for (int kb2 = 0; kb2 < 2; ++kb2) {
@@ -566,7 +582,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
                 id_f16, (kb | st) != 0);
         }
       }
-      if (!mbar_wait(bar(B_KV0 + 4), it & 1, s_abort, p.err)) return;
+      if (!mbar_wait_warp(bar(B_KV0 + 4), it & 1, s_abort, p.err)) return;
       tc_fence_after();
 #pragma unroll
       for (int st = 0; st < 4; ++st)
@@ -575,7 +591,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     };
     // O^T += V_tile^T . P^T, one commit per 128-row d_v chunk
     auto issue_pv = [&](int it) {
-      if (!mbar_wait(bar(B_PFULL), it & 1, s_abort, p.err)) return;
+      if (!mbar_wait_warp(bar(B_PFULL), it & 1, s_abort, p.err)) return;
       tc_fence_after();
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
@@ -707,10 +723,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       const int idx1 = idx_ahead;
       const int slot2 = slot + 2 * BM;
       idx_ahead = (it + 2 < ntiles && slot2 < hi) ? __ldg(idx_row + slot2) : -1;
-      if (warp == W_SOFT) {
-        if (issuer) issue_st(it);
-        __syncwarp();
-      }
+      if (warp == W_SOFT) issue_st(it);
       const bool failed = !mbar_wait(bar(B_SFULL), it & 1, s_abort, p.err);
       if (bar_or(1, 128, failed)) {
         alive = false;
@@ -797,8 +810,8 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int h = 8 * j + 2 * k;
-          const float e0 = valid ? exp2f(x[h]) : 0.f;
-          const float e1 = valid ? exp2f(x[h + 1]) : 0.f;
+          const float e0 = valid ? ex2(x[h]) : 0.f;
+          const float e1 = valid ? ex2(x[h + 1]) : 0.f;
           x[h] = e0;
           x[h + 1] = e1;
           const __half2 hv = __floats2half2_rn(e0, e1);
@@ -809,10 +822,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL));
-      if (warp == W_SOFT) {
-        if (issuer) issue_pv(it);
-        __syncwarp();
-      }
+      if (warp == W_SOFT) issue_pv(it);
       lsum0 += xreduce32_at<false, 0>(x);
       lsum1 += xreduce32_at<false, 32>(x);
       valid_next = (it + 1 < ntiles && slot + BM < hi) && resolve_row(p, btr, idx1) >= 0;
@@ -850,39 +860,89 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
         }
       }
       named_bar(1, 128);
-      // outputs straight from TMEM: per head, a warp's 32 lanes store 32
-      // consecutive d_v values (64 or 128 contiguous bytes)
+      // O^T -> registers, 32 head columns at a time -> two transpose stages
+      // through lane pairs and quads: lane l ends up with 4 consecutive d_v
+      // values (4*(l/4) .. +3 of this warp's 32) for 8 heads
+      // (hq = 32*half + 16*(l&1) + 8*((l>>1)&1) + j), stored as one 8-byte
+      // (bf16 out) or 16-byte (fp32 partial) word per head.
+      const bool odd = lane & 1, hi2 = lane & 2;
+      const bool out_al8 = ((reinterpret_cast<uintptr_t>(p.out) | (uintptr_t)(p.out_stride_t * 2)) & 7) == 0;
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        const int dv = 128 * ch + c;
-        float o[64];
+      for (int part = 0; part < 8; ++part) {
+        const int ch = part >> 1, half = part & 1;
+        const int dv0 = 128 * ch + 32 * q4 + 4 * (lane >> 2);
+        const int hq = 32 * half + 16 * (lane & 1) + 8 * ((lane >> 1) & 1);
+        float o[32];
         if (ntiles > 0) {
-          tmem_ld64(T_O + 64 * ch + lane_off, o);
+          tmem_ld16(T_O + 64 * ch + 32 * half + lane_off, o);
+          tmem_ld16(T_O + 64 * ch + 32 * half + 16 + lane_off, o + 16);
+          tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int h = 0; h < 64; ++h) o[h] = 0.f;
+          for (int h = 0; h < 32; ++h) o[h] = 0.f;
         }
+#pragma unroll
+        for (int h = 0; h < 32; ++h) o[h] *= s_alpha[32 * half + h];
         if (final_out) {
-          __nv_bfloat16* ob = p.out + (int64_t)t * p.out_stride_t + (int64_t)h0 * kDV + dv;
+          uint32_t wv[16];
 #pragma unroll
-          for (int h = 0; h < 64; ++h) ob[(int64_t)h * kDV] = __float2bfloat16_rn(o[h] * s_alpha[h]);
+          for (int j = 0; j < 16; ++j) {
+            const float send = odd ? o[j] : o[16 + j];
+            const float keep = odd ? o[16 + j] : o[j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const __nv_bfloat162 bv = odd ? __floats2bfloat162_rn(recv, keep) : __floats2bfloat162_rn(keep, recv);
+            wv[j] = *reinterpret_cast<const uint32_t*>(&bv);
+          }
+          __nv_bfloat16* ob = p.out + (int64_t)t * p.out_stride_t + (int64_t)(h0 + hq) * kDV + dv0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t send = hi2 ? wv[j] : wv[8 + j];
+            const uint32_t keep = hi2 ? wv[8 + j] : wv[j];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+            const uint2 st = hi2 ? make_uint2(recv, keep) : make_uint2(keep, recv);
+            if (out_al8) {
+              *reinterpret_cast<uint2*>(ob + (int64_t)j * kDV) = st;
+            } else {
+              unsigned short* os = reinterpret_cast<unsigned short*>(ob + (int64_t)j * kDV);
+              os[0] = (unsigned short)(st.x & 0xFFFFu);
+              os[1] = (unsigned short)(st.x >> 16);
+              os[2] = (unsigned short)(st.y & 0xFFFFu);
+              os[3] = (unsigned short)(st.y >> 16);
+            }
+          }
         } else {
-          float* wb = p.ws_o + (((int64_t)t * p.H + h0) * p.num_splits + split) * kDV + dv;
+          float2 f2[16];
 #pragma unroll
-          for (int h = 0; h < 64; ++h) wb[(int64_t)h * p.num_splits * kDV] = o[h] * s_alpha[h];
+          for (int j = 0; j < 16; ++j) {
+            const float send = odd ? o[j] : o[16 + j];
+            const float keep = odd ? o[16 + j] : o[j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            f2[j] = odd ? make_float2(recv, keep) : make_float2(keep, recv);
+          }
+          const int64_t hstride = (int64_t)p.num_splits * kDV;
+          float* wb = p.ws_o + (((int64_t)t * p.H + h0 + hq) * p.num_splits + split) * kDV + dv0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float2 send = hi2 ? f2[j] : f2[8 + j];
+            const float2 keep = hi2 ? f2[8 + j] : f2[j];
+            float2 recv;
+            recv.x = __shfl_xor_sync(0xffffffffu, send.x, 2);
+            recv.y = __shfl_xor_sync(0xffffffffu, send.y, 2);
+            const float4 st = hi2 ? make_float4(recv.x, recv.y, keep.x, keep.y)
+                                  : make_float4(keep.x, keep.y, recv.x, recv.y);
+            *reinterpret_cast<float4*>(wb + (int64_t)j * hstride) = st;
+          }
         }
       }
     }
     if (warp == W_SOFT) {
-      if (issuer) {
-        // every issued MMA completes before TMEM is released
-        mma_commit(bar(B_DRAIN));
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(bar(B_DRAIN), 0)) {
-          if (globaltimer() - t0 > kTimeoutNs) {
-            atomicOr(p.err, kErrTimeout);
-            break;
-          }
+      // every issued MMA completes before TMEM is released
+      mma_commit(bar(B_DRAIN));
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(bar(B_DRAIN), 0)) {
+        if (globaltimer() - t0 > kTimeoutNs) {
+          if (lane == 0) atomicOr(p.err, kErrTimeout);
+          break;
         }
       }
       __syncwarp();
