@@ -45,8 +45,9 @@ namespace tc_path {
 
 constexpr int BM = 128;  // candidate rows per tile (MMA M)
 constexpr int HG = 64;   // heads per CTA (MMA N)
-constexpr int NT = 384;   // 8 producer warps, 4 softmax warps
+constexpr int NT = 512;   // 8 producer warps, 4 softmax warps, 1 MMA warp, 3 idle
 constexpr int W_SOFT = 8;
+constexpr int W_MMA = 12;
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 
 // shared memory map (offsets from a 1024-aligned base)
@@ -65,7 +66,7 @@ constexpr int SMEM_USED = OFF_MISC + 256;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;      // + alignment slack
 
 // barrier slots in OFF_MISC (8 bytes each)
-enum { B_KV0 = 0, B_SFULL = 5, B_PFULL = 6, B_PV0 = 7, B_DRAIN = 11, B_QRAW = 12, B_QCONV = 13, N_BARS = 14 };
+enum { B_KV0 = 0, B_SFULL = 5, B_PFULL = 6, B_PV0 = 7, B_DRAIN = 11, B_QCONV = 12, N_BARS = 13 };
 constexpr int OFF_FLAGS = OFF_MISC + N_BARS * 8;  // int abort, int rescale, uint32 tmem base
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -90,7 +91,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait.  Returns false if the CTA is aborting (timeout here or elsewhere).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
@@ -210,6 +211,12 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 // Byte offset of 16-byte chunk `ch` of row `r` inside a [rows x 128 B] SW128 block.
 __device__ __forceinline__ uint32_t sw128(int r, int ch) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4));
+}
+
+// Offset in the q buffer of the 16-byte chunk j (dims 8j .. 8j+7) of head row hh.
+__device__ __forceinline__ uint32_t q_chunk_off(int hh, int j) {
+  return j < 64 ? (uint32_t)(OFF_Q + (j >> 3) * 8192) + sw128(hh, j & 7)
+                : (uint32_t)(OFF_Q + 8 * 8192) + sw128(hh, j - 64);
 }
 
 // Warp transpose-reduction of 64 per-lane values: lane l receives the
@@ -420,8 +427,6 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
     }
   };
   if (ntiles > 0) issue(0);
-  // the tile buffer holds the raw q until the softmax warps have converted it
-  if (ntiles > 0 && !mbar_wait(bars + 8u * B_QCONV, 0, s_abort, p.err)) return;
   for (int it = 0; it < ntiles; ++it) {
     // scales of the 16 rows (invalid rows have zero data and zero scale)
 #pragma unroll
@@ -524,27 +529,10 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       mbar_init(bar(B_PFULL), 128);
       for (int c = 0; c < 4; ++c) mbar_init(bar(B_PV0 + c), 1);
       mbar_init(bar(B_DRAIN), 1);
-      mbar_init(bar(B_QRAW), 1);
       mbar_init(bar(B_QCONV), 128);
       *s_abort = 0;
       *s_flag = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-      // raw q rows of this token's head group (64 x 1152 contiguous bytes) ->
-      // the tile buffer, with one bulk copy per 8 KB
-      const __nv_bfloat16* qsrc = p.q + (int64_t)t * p.q_stride_t + (int64_t)h0 * kDQK;
-      const bool bulk = (reinterpret_cast<uintptr_t>(qsrc) & 15) == 0;
-      *(volatile int*)(smem + OFF_FLAGS + 12) = bulk ? 1 : 0;
-      if (bulk) {
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar(B_QRAW)), "r"(HG * kDQK * 2)
-                     : "memory");
-#pragma unroll 1
-        for (int k = 0; k < 9; ++k)
-          asm volatile(
-              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 8192, [%2];" ::"r"(
-                  sbase + OFF_TILE + k * 8192),
-              "l"(reinterpret_cast<const uint8_t*>(qsrc) + k * 8192), "r"(bar(B_QRAW))
-              : "memory");
-      }
     }
     __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(s_tmem))
@@ -560,64 +548,106 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
 
   if (warp < W_SOFT) {
     // ============================================================ producers
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 136;" ::: "memory");
     producer(p, smem, sbase, bars, t, lo, hi, ntiles, warp, lane, s_abort);
-  } else {
-    // ============================================================ softmax (+ MMA issue)
-    const int q4 = warp & 3;
-    const uint32_t id_f16 = idesc(0, 0, 0);
-    const uint32_t id_bf16 = idesc(1, 0, 0);
-    const uint32_t id_pv = idesc(0, 1, 1);
-    const uint32_t a_tile = sbase + OFF_TILE, a_rope = sbase + OFF_ROPE, b_q = sbase + OFF_Q;
-    // S^T(it) = K_tile . Q^T, 128-dim group by group as the producers finish them
-    auto issue_st = [&](int it) {
-      for (int g = 0; g < 4; ++g) {
-        if (!mbar_wait_warp(bar(B_KV0 + g), it & 1, s_abort, p.err)) return;
+  } else if (warp >= W_MMA) {
+    // ============================================================ MMA issue (warp 12; 13-15 idle)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    if (warp == W_MMA) {
+      const uint32_t id_f16 = idesc(0, 0, 0);
+      const uint32_t id_bf16 = idesc(1, 0, 0);
+      const uint32_t id_pv = idesc(0, 1, 1);
+      const uint32_t a_tile = sbase + OFF_TILE, a_rope = sbase + OFF_ROPE, b_q = sbase + OFF_Q;
+      // S^T(it) = K_tile . Q^T, 128-dim group by group as the producers finish them
+      auto issue_st = [&](int it) -> bool {
+        for (int g = 0; g < 4; ++g) {
+          if (!mbar_wait_warp(bar(B_KV0 + g), it & 1, s_abort, p.err)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kb2 = 0; kb2 < 2; ++kb2) {
+            const int kb = 2 * g + kb2;
+#pragma unroll
+            for (int st = 0; st < 4; ++st)
+              mma(T_S, sdesc(a_tile + kb * 16384 + st * 32, 16, 1024), sdesc(b_q + kb * 8192 + st * 32, 16, 1024),
+                  id_f16, (kb | st) != 0);
+          }
+        }
+        if (!mbar_wait_warp(bar(B_KV0 + 4), it & 1, s_abort, p.err)) return false;
         tc_fence_after();
 #pragma unroll
-        for (int kb2 = 0; kb2 < 2; ++kb2) {
-          const int kb = 2 * g + kb2;
+        for (int st = 0; st < 4; ++st)
+          mma(T_S, sdesc(a_rope + st * 32, 16, 1024), sdesc(b_q + 8 * 8192 + st * 32, 16, 1024), id_bf16, 1);
+        mma_commit(bar(B_SFULL));
+        return true;
+      };
+      // O^T += V_tile^T . P^T, one commit per 128-row d_v chunk
+      auto issue_pv = [&](int it) -> bool {
+        if (!mbar_wait_warp(bar(B_PFULL), it & 1, s_abort, p.err)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
 #pragma unroll
-          for (int st = 0; st < 4; ++st)
-            mma(T_S, sdesc(a_tile + kb * 16384 + st * 32, 16, 1024), sdesc(b_q + kb * 8192 + st * 32, 16, 1024),
-                id_f16, (kb | st) != 0);
+          for (int ks = 0; ks < 8; ++ks)
+            mma(T_O + 64 * ch, sdesc(a_tile + 2 * ch * 16384 + ks * 2048, 16384, 1024),
+                sdesc(a_rope + ks * 2048, 8192, 1024), id_pv, (it > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar(B_PV0 + ch));
+        }
+        return true;
+      };
+      const bool q_ok = ntiles == 0 || mbar_wait_warp(bar(B_QCONV), 0, s_abort, p.err);
+      for (int it = 0; it < ntiles && q_ok; ++it) {
+        if (!issue_st(it)) break;
+        if (!issue_pv(it)) break;
+      }
+      // every issued MMA completes before TMEM is released
+      mma_commit(bar(B_DRAIN));
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(bar(B_DRAIN), 0)) {
+        if (globaltimer() - t0 > kTimeoutNs) {
+          if (lane == 0) atomicOr(p.err, kErrTimeout);
+          break;
         }
       }
-      if (!mbar_wait_warp(bar(B_KV0 + 4), it & 1, s_abort, p.err)) return;
-      tc_fence_after();
-#pragma unroll
-      for (int st = 0; st < 4; ++st)
-        mma(T_S, sdesc(a_rope + st * 32, 16, 1024), sdesc(b_q + 8 * 8192 + st * 32, 16, 1024), id_bf16, 1);
-      mma_commit(bar(B_SFULL));
-    };
-    // O^T += V_tile^T . P^T, one commit per 128-row d_v chunk
-    auto issue_pv = [&](int it) {
-      if (!mbar_wait_warp(bar(B_PFULL), it & 1, s_abort, p.err)) return;
-      tc_fence_after();
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma(T_O + 64 * ch, sdesc(a_tile + 2 * ch * 16384 + ks * 2048, 16384, 1024),
-              sdesc(a_rope + ks * 2048, 8192, 1024), id_pv, (it > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(bar(B_PV0 + ch));
-      }
-    };
+      __syncwarp();
+    }
+  } else {
+    // ============================================================ softmax + epilogue
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
+    const int q4 = warp & 3;
     const int c = q4 * 32 + lane;  // TMEM lane: candidate (S^T) / dv row (O^T)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    // q of this token (while the producers gather the first tile).
-    const bool bulk = *(volatile int*)(smem + OFF_FLAGS + 12) != 0;
-    if (bulk) {
-      // raw bf16 q sits in the tile buffer: thread c handles head c/2, 16-byte
-      // chunks [36 (c%2), 36 (c%2) + 36) of its 72
-      const int hh = c >> 1, half = c & 1;
-      const uint8_t* raw = smem + OFF_TILE + hh * (kDQK * 2) + half * 36 * 16;
-      if (!mbar_wait(bar(B_QRAW), 0, s_abort, p.err)) {
-        // abort: the tile loop below sees the flag
+    // the sinks of this warp's two heads (warp 8 computes the normalisers),
+    // read now so that the load is long done by the epilogue
+    const float sink_lo = (q4 == 0 && p.attn_sink) ? __ldg(p.attn_sink + h0 + lane) : 0.f;
+    const float sink_hi = (q4 == 0 && p.attn_sink) ? __ldg(p.attn_sink + h0 + lane + 32) : 0.f;
+    // q of this token, while the producers gather the first tile: the 64 head
+    // rows (one contiguous 72 KB block) are copied into their swizzled places
+    // in the q buffer by coalesced 16-byte cp.async, then converted in place;
+    // thread c converts head c/2, chunks [36 (c%2), 36 (c%2) + 36) of its 72.
+    {
+      const __nv_bfloat16* qsrc = p.q + (int64_t)t * p.q_stride_t + (int64_t)h0 * kDQK;
+      if ((reinterpret_cast<uintptr_t>(qsrc) & 15) == 0) {
+#pragma unroll 4
+        for (int f = c; f < HG * 72; f += 128) cp_async16(sbase + q_chunk_off(f / 72, f % 72), qsrc + 8 * f, 16);
+        cp_async_commit();
+        cp_async_wait<0>();
+      } else {
+        const unsigned short* qs = reinterpret_cast<const unsigned short*>(qsrc);
+#pragma unroll 2
+        for (int f = c; f < HG * 72; f += 128) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w[i] = (uint32_t)__ldg(qs + 8 * f + 2 * i) | ((uint32_t)__ldg(qs + 8 * f + 2 * i + 1) << 16);
+          sts128(sbase + q_chunk_off(f / 72, f % 72), make_uint4(w[0], w[1], w[2], w[3]));
+        }
       }
+      named_bar(1, 128);
+      const int hh = c >> 1, half = c & 1;
       float amax = 0.f;
 #pragma unroll 4
       for (int k = 0; k < 36; ++k) {
-        const uint4 v = *reinterpret_cast<const uint4*>(raw + k * 16);
+        const uint4 v = *reinterpret_cast<const uint4*>(smem + q_chunk_off(hh, 36 * half + k));
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -631,7 +661,8 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
 #pragma unroll 4
       for (int k = 0; k < 36; ++k) {
         const int ch = 36 * half + k;  // 8 dims: 8ch .. 8ch+7
-        const uint4 v = *reinterpret_cast<const uint4*>(raw + k * 16);
+        const uint32_t off = q_chunk_off(hh, ch);
+        const uint4 v = *reinterpret_cast<const uint4*>(smem + off);
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[4];
 #pragma unroll
@@ -646,8 +677,6 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
             o[i] = *reinterpret_cast<const uint32_t*>(&bv);
           }
         }
-        const uint32_t off = ch < 64 ? OFF_Q + (ch >> 3) * 8192 + sw128(hh, ch & 7)
-                                     : OFF_Q + 8 * 8192 + sw128(hh, ch - 64);
         sts128(sbase + off, make_uint4(o[0], o[1], o[2], o[3]));
       }
       if (half == 0) {
@@ -655,54 +684,9 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
         s_mref[hh] = -INFINITY;
         s_mneg[hh] = 0.f;
       }
-    } else {
-      // q rows not 16-byte aligned: load through registers, warp q4 converts
-      // heads 16 q4 .. +15 in two rounds of 8 (lane l: head l/4, chunks l%4 + 4k)
-#pragma unroll 1
-      for (int round = 0; round < 2; ++round) {
-        const int hh = 16 * q4 + 8 * round + (lane >> 2);
-        const int sub = lane & 3;
-        const unsigned short* qrow = reinterpret_cast<const unsigned short*>(
-            p.q + (int64_t)t * p.q_stride_t + (int64_t)(h0 + hh) * kDQK);
-        float amax = 0.f;
-#pragma unroll 1
-        for (int k = 0; k < 18; ++k)
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)__ldg(qrow + (sub + 4 * k) * 8 + i) << 16)));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const int e = q_prescale_exp(amax);
-        const float down = pow2f(-e);
-#pragma unroll 1
-        for (int k = 0; k < 18; ++k) {
-          const int ch = sub + 4 * k;
-          uint32_t o[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float a = __uint_as_float((uint32_t)__ldg(qrow + ch * 8 + 2 * i) << 16) * down;
-            const float b = __uint_as_float((uint32_t)__ldg(qrow + ch * 8 + 2 * i + 1) << 16) * down;
-            if (ch < 64) {
-              const __half2 hv = __floats2half2_rn(a, b);
-              o[i] = *reinterpret_cast<const uint32_t*>(&hv);
-            } else {
-              const __nv_bfloat162 bv = __floats2bfloat162_rn(a, b);
-              o[i] = *reinterpret_cast<const uint32_t*>(&bv);
-            }
-          }
-          const uint32_t off = ch < 64 ? OFF_Q + (ch >> 3) * 8192 + sw128(hh, ch & 7)
-                                       : OFF_Q + 8 * 8192 + sw128(hh, ch - 64);
-          sts128(sbase + off, make_uint4(o[0], o[1], o[2], o[3]));
-        }
-        if (sub == 0) {
-          s_qmul[hh] = p.sm_scale * kLog2e * pow2f(e);
-          s_mref[hh] = -INFINITY;
-          s_mneg[hh] = 0.f;
-        }
-      }
     }
     fence_proxy_async();
-    mbar_arrive(bar(B_QCONV));  // the tile buffer is free for the producers
+    mbar_arrive(bar(B_QCONV));  // q is ready for the S^T MMAs
     named_bar(1, 128);  // q, s_qmul and s_mref visible to all softmax warps and the issuer
 
     // running sums of P per head: lane l keeps heads l and l+32 of this warp's
@@ -723,7 +707,6 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       const int idx1 = idx_ahead;
       const int slot2 = slot + 2 * BM;
       idx_ahead = (it + 2 < ntiles && slot2 < hi) ? __ldg(idx_row + slot2) : -1;
-      if (warp == W_SOFT) issue_st(it);
       const bool failed = !mbar_wait(bar(B_SFULL), it & 1, s_abort, p.err);
       if (bar_or(1, 128, failed)) {
         alive = false;
@@ -822,7 +805,6 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL));
-      if (warp == W_SOFT) issue_pv(it);
       lsum0 += xreduce32_at<false, 0>(x);
       lsum1 += xreduce32_at<false, 32>(x);
       valid_next = (it + 1 < ntiles && slot + BM < hi) && resolve_row(p, btr, idx1) >= 0;
@@ -848,7 +830,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
           const float lse_v = lt > 0.f ? (mu + log2f(lt)) * kLn2 : -INFINITY;
           float inv;
           if (final_out) {
-            const float sk = p.attn_sink ? exp2f(__ldg(p.attn_sink + h) * kLog2e - mu) : 0.f;
+            const float sk = p.attn_sink ? exp2f((j == 0 ? sink_lo : sink_hi) * kLog2e - mu) : 0.f;
             const float den = lt + sk;
             inv = den > 0.f ? 1.f / den : 0.f;
             p.lse[(int64_t)t * p.lse_stride_t + h] = lse_v;
@@ -882,7 +864,13 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
           for (int h = 0; h < 32; ++h) o[h] = 0.f;
         }
 #pragma unroll
-        for (int h = 0; h < 32; ++h) o[h] *= s_alpha[32 * half + h];
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(s_alpha + 32 * half + 4 * h4);
+          o[4 * h4 + 0] *= a4.x;
+          o[4 * h4 + 1] *= a4.y;
+          o[4 * h4 + 2] *= a4.z;
+          o[4 * h4 + 3] *= a4.w;
+        }
         if (final_out) {
           uint32_t wv[16];
 #pragma unroll
@@ -934,18 +922,6 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
           }
         }
       }
-    }
-    if (warp == W_SOFT) {
-      // every issued MMA completes before TMEM is released
-      mma_commit(bar(B_DRAIN));
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(bar(B_DRAIN), 0)) {
-        if (globaltimer() - t0 > kTimeoutNs) {
-          if (lane == 0) atomicOr(p.err, kErrTimeout);
-          break;
-        }
-      }
-      __syncwarp();
     }
   }
   tc_fence_before();
