@@ -35,18 +35,23 @@ UNIT = "query-tokens/s"
 ROW = 656
 
 
-def workloads():
+def workloads(tokens=None):
+    """The benchmark workloads.  ``tokens`` shrinks the query-token count of a
+    prefill workload (for a small profiling case of the same kernel)."""
     from sparse_mla_attention_03_gb300 import inputs
+    T16 = tokens or 1024
+    TF = tokens or 8192
+    TL = tokens or 4096
     return {
-        "prefill16k": dict(name="prefill_T1024_H64_ctx16384_k512+k1024", kind="prefill", bound="tensor",
-                           parts=[("k512", lambda s: inputs.prefill_16k(512, seed=s)),
-                                  ("k1024", lambda s: inputs.prefill_16k(1024, seed=s))]),
-        "fewhead": dict(name="fewhead_prefill_T8192_H8_ctx32768_k640_ld1024_ragged", kind="prefill",
-                        bound="hbm", parts=[("all", lambda s: inputs.fewhead_prefill(seed=s))]),
+        "prefill16k": dict(name=f"prefill_T{T16}_H64_ctx16384_k512+k1024", kind="prefill", bound="tensor",
+                           parts=[("k512", lambda s: inputs.prefill_16k(512, seed=s, T=T16)),
+                                  ("k1024", lambda s: inputs.prefill_16k(1024, seed=s, T=T16))]),
+        "fewhead": dict(name=f"fewhead_prefill_T{TF}_H8_ctx32768_k640_ld1024_ragged", kind="prefill",
+                        bound="hbm", parts=[("all", lambda s: inputs.fewhead_prefill(seed=s, T=TF))]),
         "decode": dict(name="decode_64req_x2_H64_ctx32768_k2048_paged", kind="decode", bound="hbm",
                        parts=[("all", lambda s: inputs.batched_decode(seed=s))]),
-        "large": dict(name="large_prefill_T4096_H128_ctx131072_k2048_neg0.1", kind="prefill", bound="tensor",
-                      parts=[("all", lambda s: inputs.large_prefill(seed=s))]),
+        "large": dict(name=f"large_prefill_T{TL}_H128_ctx131072_k2048_neg0.1", kind="prefill", bound="tensor",
+                      parts=[("all", lambda s: inputs.large_prefill(seed=s, T=TL))]),
         "tiny": dict(name="tiny_prefill_T4_H8_ctx256_k64", kind="prefill", bound="hbm",
                      parts=[("all", lambda s: inputs.tiny_prefill(seed=s))]),
     }
@@ -227,7 +232,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     binding.load()
-    spec = workloads()[args.workload]
+    spec = workloads(args.tokens)[args.workload]
     peaks = load_peaks()
     parts = []
     for tag, mk in spec["parts"]:
@@ -362,7 +367,7 @@ def cpu_baseline(parts_or_wls, budget_tokens):
 
 def run_reference(args):
     """The CPU oracle as the reference arm: each step is a bounded token sample."""
-    spec = workloads()[args.workload]
+    spec = workloads(args.tokens)[args.workload]
     wls = [mk(args.seed) for _, mk in spec["parts"]]
     budget = args.ref_tokens
     cores = min(host_cores(), 32)
@@ -402,6 +407,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample per part for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=128, help="oracle sample per part per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="query tokens of a prefill workload (smaller profiling case; default: the full workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
