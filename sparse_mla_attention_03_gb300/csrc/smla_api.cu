@@ -126,6 +126,25 @@ int splits_for(int T, int H, int topk, int num_splits, int num_sms) {
   int S;
   if (num_splits > 0) {
     S = num_splits < chunks ? num_splits : chunks;
+  } else if (smla::tc_supported(H)) {
+    // tcgen05 kernel: one CTA per SM, each paying a fixed cost (q load, first
+    // gather latency, epilogue: about 2.5 tiles' worth) plus one unit per
+    // 128-row tile.  Pick the split count with the fewest waves x CTA length.
+    const int sms = num_sms > 0 ? num_sms : 148;
+    const int64_t base = (int64_t)T * (H / 64);
+    double best = 0.0;
+    S = 1;
+    for (int s = 1; s <= SMLA_MAX_SPLITS && s <= chunks; ++s) {
+      const int per = (chunks + s - 1) / s;               // 64-slot chunks per split
+      if (s > 1 && (chunks + per - 1) / per < s) continue;  // same partition as a smaller s
+      const int64_t ctas = base * s;
+      const double waves = (double)((ctas + sms - 1) / sms);
+      const double cost = waves * (2.5 + (per + 1) / 2);
+      if (s == 1 || cost < best * 0.97) {
+        best = cost;
+        S = s;
+      }
+    }
   } else {
     const int hpc = smla::heads_per_cta(H);
     const int64_t base = (int64_t)T * ((H + hpc - 1) / hpc);

@@ -41,11 +41,14 @@ __device__ __forceinline__ int swz(int row, int ch) {
   return ch < 40 ? (ch ^ (((row >> 2) & 3) << 1)) : ch;
 }
 
-template <int NH8>
+// NST staged tiles: 2 overlap a CTA's own gather with its compute; 1 halves
+// the CTA's shared memory so that 4 CTAs (16 warps) share an SM and hide the
+// gather latency across CTAs instead.
+template <int NH8, int NST>
 struct Layout {
   static constexpr int HG = NH8 * 8;
   static constexpr int kv = 0;
-  static constexpr int q = 2 * BC * TS;
+  static constexpr int q = NST * BC * TS;
   static constexpr int p = q + HG * QS;
   static constexpr int red = p + HG * PS;
   static constexpr int lsum = red + 4 * HG * 4;
@@ -60,10 +63,10 @@ __device__ __forceinline__ uint32_t wsel(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
-template <int NH8>
-__global__ void __launch_bounds__(NT, 2) mma_kernel(const KParams p) {
+template <int NH8, int NST>
+__global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams p) {
   constexpr int HG = NH8 * 8;
-  using L = Layout<NH8>;
+  using L = Layout<NH8, NST>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
@@ -162,15 +165,20 @@ __global__ void __launch_bounds__(NT, 2) mma_kernel(const KParams p) {
   __syncthreads();  // q visible
   if (ntiles > 0) vmask[0] = issue(0, 0);
   cp_async_commit();
-  if (ntiles > 1) vmask[1] = issue(1, 1);
-  cp_async_commit();
+  if (NST == 2) {
+    if (ntiles > 1) vmask[1] = issue(1, 1);
+    cp_async_commit();
+  }
 
   const int rg = warp * 16 + g, rg8 = rg + 8;
   uint8_t* s_p = smem + L::p;
 
   for (int it = 0; it < ntiles; ++it) {
-    const int st = it & 1;
-    cp_async_wait<1>();
+    const int st = NST == 2 ? (it & 1) : 0;
+    if (NST == 2)
+      cp_async_wait<1>();
+    else
+      cp_async_wait<0>();
     __syncthreads();
     const uint8_t* tile = smem + L::kv + st * BC * TS;
     const uint8_t* pg = tile + rg * TS;
@@ -343,7 +351,7 @@ __global__ void __launch_bounds__(NT, 2) mma_kernel(const KParams p) {
       }
     }
     __syncthreads();  // stage st and P are free
-    if (it + 2 < ntiles) vmask[st] = issue(it + 2, st);
+    if (it + NST < ntiles) vmask[st] = issue(it + NST, st);
     cp_async_commit();
   }
   cp_async_wait<0>();
@@ -406,16 +414,16 @@ __global__ void __launch_bounds__(NT, 2) mma_kernel(const KParams p) {
   }
 }
 
-template <int NH8>
+template <int NH8, int NST>
 static cudaError_t launch(const KParams& p, cudaStream_t stream) {
-  using L = Layout<NH8>;
+  using L = Layout<NH8, NST>;
   const int n_hg = (p.H + NH8 * 8 - 1) / (NH8 * 8);
   const int64_t grid = (int64_t)p.T * n_hg * p.num_splits;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(mma_kernel<NH8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
+  cudaError_t e = cudaFuncSetAttribute(mma_kernel<NH8, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
   if (e != cudaSuccess) return e;
-  mma_kernel<NH8><<<(unsigned)grid, NT, L::total, stream>>>(p);
+  mma_kernel<NH8, NST><<<(unsigned)grid, NT, L::total, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -424,7 +432,7 @@ static cudaError_t launch(const KParams& p, cudaStream_t stream) {
 int mma_heads_per_cta(int H) { return H <= 8 ? 8 : 16; }
 
 cudaError_t launch_mma(const KParams& p, cudaStream_t stream) {
-  return mma_heads_per_cta(p.H) == 8 ? mma_path::launch<1>(p, stream) : mma_path::launch<2>(p, stream);
+  return mma_heads_per_cta(p.H) == 8 ? mma_path::launch<1, 1>(p, stream) : mma_path::launch<2, 2>(p, stream);
 }
 
 }  // namespace smla
