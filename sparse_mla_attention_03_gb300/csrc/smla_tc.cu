@@ -156,6 +156,22 @@ __host__ __device__ constexpr uint32_t idesc(uint32_t fmt, uint32_t a_major, uin
   return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_major << 15) | (b_major << 16) | ((uint32_t)(HG >> 3) << 17) |
          ((uint32_t)(BM >> 4) << 24);
 }
+// The same descriptor split in its two 32-bit words: the low word holds the
+// start address >> 4 and the leading byte offset >> 4; the high word (stride
+// 1024 B between 8-row groups, version bit 46, 128-byte swizzle) is the same
+// for every operand here.  Advancing an operand is then one 32-bit add.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ void mma_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n .reg .b64 da, db;\n setp.ne.b32 p, %4, 0;\n mov.b64 da, {%1, %5};\n"
+      " mov.b64 db, {%2, %5};\n elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(id), "r"(acc), "r"(kDescHi)
+      : "memory");
+}
 // One MMA issued by one elected lane of a converged warp.
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
   asm volatile(
@@ -557,26 +573,31 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       const uint32_t id_f16 = idesc(0, 0, 0);
       const uint32_t id_bf16 = idesc(1, 0, 0);
       const uint32_t id_pv = idesc(0, 1, 1);
-      const uint32_t a_tile = sbase + OFF_TILE, a_rope = sbase + OFF_ROPE, b_q = sbase + OFF_Q;
+      const uint32_t ad_tile = sdesc_lo(sbase + OFF_TILE, 16);      // K-major view (S^T)
+      const uint32_t ad_tile_mn = sdesc_lo(sbase + OFF_TILE, 16384);  // MN-major view (PV)
+      const uint32_t ad_rope = sdesc_lo(sbase + OFF_ROPE, 16);
+      const uint32_t bd_p = sdesc_lo(sbase + OFF_ROPE, 8192);
+      const uint32_t bd_q = sdesc_lo(sbase + OFF_Q, 16);
       // S^T(it) = K_tile . Q^T, 128-dim group by group as the producers finish them
       auto issue_st = [&](int it) -> bool {
+#pragma unroll 1
         for (int g = 0; g < 4; ++g) {
           if (!mbar_wait_warp(bar(B_KV0 + g), it & 1, s_abort, p.err)) return false;
           tc_fence_after();
+          uint32_t ag = ad_tile + (uint32_t)g * (2 * 16384 >> 4), bg = bd_q + (uint32_t)g * (2 * 8192 >> 4);
+          asm volatile("" : "+r"(ag), "+r"(bg));  // keep the group's bases in registers, not its 16 operands
 #pragma unroll
-          for (int kb2 = 0; kb2 < 2; ++kb2) {
-            const int kb = 2 * g + kb2;
+          for (int kb2 = 0; kb2 < 2; ++kb2)
 #pragma unroll
             for (int st = 0; st < 4; ++st)
-              mma(T_S, sdesc(a_tile + kb * 16384 + st * 32, 16, 1024), sdesc(b_q + kb * 8192 + st * 32, 16, 1024),
-                  id_f16, (kb | st) != 0);
-          }
+              mma_lo(T_S, ag + (uint32_t)((kb2 * 16384 + st * 32) >> 4), bg + (uint32_t)((kb2 * 8192 + st * 32) >> 4),
+                     id_f16, (g | kb2 | st) != 0);
         }
         if (!mbar_wait_warp(bar(B_KV0 + 4), it & 1, s_abort, p.err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int st = 0; st < 4; ++st)
-          mma(T_S, sdesc(a_rope + st * 32, 16, 1024), sdesc(b_q + 8 * 8192 + st * 32, 16, 1024), id_bf16, 1);
+          mma_lo(T_S, ad_rope + (uint32_t)((st * 32) >> 4), bd_q + (uint32_t)((8 * 8192 + st * 32) >> 4), id_bf16, 1);
         mma_commit(bar(B_SFULL));
         return true;
       };
@@ -584,12 +605,14 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       auto issue_pv = [&](int it) -> bool {
         if (!mbar_wait_warp(bar(B_PFULL), it & 1, s_abort, p.err)) return false;
         tc_fence_after();
+        const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t ac = ad_tile_mn + (uint32_t)ch * (2 * 16384 >> 4);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma(T_O + 64 * ch, sdesc(a_tile + 2 * ch * 16384 + ks * 2048, 16384, 1024),
-                sdesc(a_rope + ks * 2048, 8192, 1024), id_pv, (it > 0 || ks > 0) ? 1u : 0u);
+            mma_lo(T_O + 64 * ch, ac + (uint32_t)((ks * 2048) >> 4), bd_p + (uint32_t)((ks * 2048) >> 4), id_pv,
+                   ks > 0 ? 1u : acc0);
           mma_commit(bar(B_PV0 + ch));
         }
         return true;
