@@ -303,7 +303,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8e4m3 KV / bf16 q in; f16 MMA operands, f32 accumulate; bf16 out",
+        "dtype": "f16",
+        "precision": "fp8 e4m3 cache and bf16 q in; f16 MMA operands with fp32 accumulation; bf16 out, fp32 lse",
         "data": "synthetic (seeded numpy PCG64; no dataset or weights involved)",
         "config": {"workload": spec["name"], "global_batch_tokens": tokens_per_step * world,
                    "parallelism": f"dp{world} (independent token shards, no collective)",
@@ -404,7 +405,7 @@ def main():
                     default="prefill16k")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample per part for cpu_baseline")
+    ap.add_argument("--cpu-tokens", type=int, default=512, help="oracle sample per part for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=128, help="oracle sample per part per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=None,
