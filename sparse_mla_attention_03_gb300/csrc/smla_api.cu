@@ -26,6 +26,7 @@ __device__ int g_error_word;
 constexpr int kMaxDevices = 64;
 int* g_err_ptr[kMaxDevices];
 int g_num_sms[kMaxDevices];
+int64_t g_l2_bytes[kMaxDevices];
 std::mutex g_dev_mu;
 
 int device_setup(int* dev_out) {
@@ -40,7 +41,11 @@ int device_setup(int* dev_out) {
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    int l2 = 0;
+    e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
     g_num_sms[dev] = sms;
+    g_l2_bytes[dev] = l2;
     g_err_ptr[dev] = ptr;
   }
   *dev_out = dev;
@@ -114,6 +119,10 @@ smla::KParams make_params(const smla_args* a, int dev) {
   p.lse_stride_t = a->lse_stride_t;
   p.num_splits = 1;
   p.split_len = ((a->topk + 63) / 64) * 64;
+  // The gathered rows of a cache within a quarter of L2 are re-read from L2
+  // after their first touch, and a prefetch there only costs issue slots; a
+  // larger cache (long-context decode, 100k-token prefill) is prefetched.
+  p.l2_prefetch = (int64_t)a->num_pages * SMLA_PAGE * SMLA_ROW_BYTES > g_l2_bytes[dev] / 4 ? 1 : 0;
   p.err = g_err_ptr[dev];
   return p;
 }

@@ -411,19 +411,31 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
   // swizzles put its 8 chunks in 8 distinct bank groups.
   uint4 nope[4][4];
   uint4 tail[5];     // flat (row, chunk) f = 32k + lane: row f/9, chunk 32 + f%9
-  // index reads run one tile ahead of the row loads (lanes 0..15: one row each)
+  // index reads (lanes 0..15: one row each)
   auto load_idx = [&](int it) -> int {
     const int slot = lo + it * BM + 16 * pw + lane;
     return (lane < 16 && it < ntiles && slot < hi) ? __ldg(idx_row + slot) : -1;
   };
-  int idx_next = load_idx(0);
+  // slot indices run two tiles ahead of the row loads.  With l2_prefetch set
+  // (a cache too large to stay L2-resident) the rows of tile it+1 are
+  // prefetched into L2 while tile it is loaded, so that the row loads see L2
+  // latency and only the prefetch waits on HBM.
+  int idx_cur = load_idx(0), idx_nx = load_idx(1);
   auto issue = [&](int it) {
     int rowid = -1;
-    const int idx = idx_next;
-    idx_next = load_idx(it + 1);
+    const int idx = idx_cur, idx1 = idx_nx;
+    idx_cur = idx_nx;
+    idx_nx = load_idx(it + 2);
     if (lane < 16) {
       const int slot = lo + it * BM + 16 * pw + lane;
       if (slot < hi) rowid = resolve_row(p, btr, idx);
+      if (p.l2_prefetch && it + 1 < ntiles && slot + BM < hi) {
+        const int r1 = resolve_row(p, btr, idx1);
+        if (r1 >= 0)
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.kv + (int64_t)r1 * kRowBytes),
+                       "r"(kRowBytes)
+                       : "memory");
+      }
     }
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
