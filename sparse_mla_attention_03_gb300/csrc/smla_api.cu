@@ -120,9 +120,10 @@ smla::KParams make_params(const smla_args* a, int dev) {
   p.num_splits = 1;
   p.split_len = ((a->topk + 63) / 64) * 64;
   // The gathered rows of a cache within a quarter of L2 are re-read from L2
-  // after their first touch, and a prefetch there only costs issue slots; a
-  // larger cache (long-context decode, 100k-token prefill) is prefetched.
-  p.l2_prefetch = (int64_t)a->num_pages * SMLA_PAGE * SMLA_ROW_BYTES > g_l2_bytes[dev] / 4 ? 1 : 0;
+  // after their first touch; a larger cache (long-context decode, 100k-token
+  // prefill) is read mostly from HBM, which the tcgen05 kernel's producers
+  // meet with L2 prefetch and earlier register loads.
+  p.big_cache = (int64_t)a->num_pages * SMLA_PAGE * SMLA_ROW_BYTES > g_l2_bytes[dev] / 4 ? 1 : 0;
   p.err = g_err_ptr[dev];
   return p;
 }

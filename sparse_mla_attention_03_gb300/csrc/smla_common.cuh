@@ -61,7 +61,7 @@ struct KParams {
   int32_t split_len;  // slots per split, multiple of the tile width
   float* ws_o;        // [T, H, S, 512] fp32 partial outputs (normalised, sink-free)
   float* ws_lse;      // [T, H, S] fp32 partial LSE (natural log)
-  int32_t l2_prefetch; // 1: prefetch the next tile's rows into L2 (tcgen05 kernel)
+  int32_t big_cache;   // 1: cache larger than a quarter of L2 (its rows mostly come from HBM)
   int* err;           // device error word
 };
 

@@ -399,8 +399,8 @@ __device__ __forceinline__ void xreduce64(const float (&x)[64], float& r0, float
 // Producer warp pw (0..7) owns tile rows 16pw .. 16pw+15.  Its loads are
 // coalesced (4 lanes read 64 contiguous bytes of one row), and the 16 rows'
 // scale and rope chunks (9 per row) are read as 144 consecutive (row, chunk)
-// pairs.  All 21 loads per lane are issued as soon as the previous tile is
-// stored, before waiting for the previous PV.
+// pairs.
+template <bool kEarly>
 __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32_t sbase, uint32_t bars, int t,
                                          int lo, int hi, int ntiles, int pw, int lane, volatile int* s_abort) {
   const int32_t* idx_row = p.indices + (int64_t)t * p.idx_stride_t;
@@ -416,20 +416,27 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
     const int slot = lo + it * BM + 16 * pw + lane;
     return (lane < 16 && it < ntiles && slot < hi) ? __ldg(idx_row + slot) : -1;
   };
-  // slot indices run two tiles ahead of the row loads.  With l2_prefetch set
-  // (a cache too large to stay L2-resident) the rows of tile it+1 are
-  // prefetched into L2 while tile it is loaded, so that the row loads see L2
-  // latency and only the prefetch waits on HBM.
-  int idx_cur = load_idx(0), idx_nx = load_idx(1);
-  auto issue = [&](int it) {
+  // Slot indices are read two tiles ahead of the conversion.  With rows that
+  // stay in L2 (!kEarly), the next tile is loaded into registers in one burst
+  // after the current tile is stored, while the S^T tail, softmax and PV keep
+  // the producers idle.  With a cache larger than L2 can hold (kEarly), whose
+  // rows come from HBM, the next tile's row ids are resolved as the current
+  // tile starts and each 128-dim group (and the tail) is loaded as soon as
+  // the same group of the current tile is stored, so that it stays in flight
+  // for a whole tile period; the rows of the tile after that are prefetched
+  // into L2, so the register loads see L2 latency and only the prefetch waits
+  // on HBM.  (For L2-resident rows early loads only compete with the
+  // conversion for the L1/shared-memory path.)
+  int idx_a = load_idx(0), idx_b = load_idx(1);
+  auto resolve = [&](int it) -> int {
     int rowid = -1;
-    const int idx = idx_cur, idx1 = idx_nx;
-    idx_cur = idx_nx;
-    idx_nx = load_idx(it + 2);
+    const int idx = idx_a, idx1 = idx_b;
+    idx_a = idx_b;
+    idx_b = load_idx(it + 2);
     if (lane < 16) {
       const int slot = lo + it * BM + 16 * pw + lane;
       if (slot < hi) rowid = resolve_row(p, btr, idx);
-      if (p.l2_prefetch && it + 1 < ntiles && slot + BM < hi) {
+      if (kEarly && it + 1 < ntiles && slot + BM < hi) {
         const int r1 = resolve_row(p, btr, idx1);
         if (r1 >= 0)
           asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.kv + (int64_t)r1 * kRowBytes),
@@ -437,14 +444,18 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
                        : "memory");
       }
     }
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    return rowid;
+  };
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  auto load_group = [&](int g, int rowid) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int r = __shfl_sync(0xffffffffu, rowid, 8 * (j >> 1) + 2 * (lane >> 3) + ((lane >> 2) & 1));
       const uint4* src = reinterpret_cast<const uint4*>(p.kv + (int64_t)(r < 0 ? 0 : r) * kRowBytes);
-#pragma unroll
-      for (int g = 0; g < 4; ++g) nope[g][j] = r >= 0 ? __ldg(src + 8 * g + 4 * (j & 1) + (lane & 3)) : z;
+      nope[g][j] = r >= 0 ? __ldg(src + 8 * g + 4 * (j & 1) + (lane & 3)) : z;
     }
+  };
+  auto load_tail = [&](int rowid) {
 #pragma unroll
     for (int k = 0; k < 5; ++k) {
       const int f = 32 * k + lane;
@@ -454,8 +465,15 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
       tail[k] = (f < 144 && r >= 0) ? __ldg(src + 32 + (f - 9 * rr)) : z;
     }
   };
-  if (ntiles > 0) issue(0);
+  if (ntiles > 0) {
+    const int rowid = resolve(0);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) load_group(g, rowid);
+    load_tail(rowid);
+  }
   for (int it = 0; it < ntiles; ++it) {
+    const bool more = it + 1 < ntiles;
+    const int rowid_next = (kEarly && more) ? resolve(it + 1) : -1;
     // scales of the 16 rows (invalid rows have zero data and zero scale)
 #pragma unroll
     for (int k = 0; k < 5; ++k) {
@@ -512,11 +530,24 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
       }
       fence_proxy_async();
       mbar_arrive(bars + 8u * (B_KV0 + g));
+      // the registers of this group are free: start the next tile's loads
+      if (kEarly && more) {
+        if (g < 4)
+          load_group(g, rowid_next);
+        else
+          load_tail(rowid_next);
+      }
     }
-    if (it + 1 < ntiles) issue(it + 1);
+    if (!kEarly && more) {
+      const int rowid = resolve(it + 1);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) load_group(g, rowid);
+      load_tail(rowid);
+    }
   }
 }
 
+template <bool kEarly>
 __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the __shared__ array so
@@ -577,7 +608,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   if (warp < W_SOFT) {
     // ============================================================ producers
     asm volatile("setmaxnreg.inc.sync.aligned.u32 136;" ::: "memory");
-    producer(p, smem, sbase, bars, t, lo, hi, ntiles, warp, lane, s_abort);
+    producer<kEarly>(p, smem, sbase, bars, t, lo, hi, ntiles, warp, lane, s_abort);
   } else if (warp >= W_MMA) {
     // ============================================================ MMA issue (warp 12; 13-15 idle)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
@@ -975,10 +1006,11 @@ cudaError_t launch_tc(const KParams& p, cudaStream_t stream) {
   const int64_t grid = (int64_t)p.T * (p.H / tc_path::HG) * p.num_splits;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  cudaError_t e =
-      cudaFuncSetAttribute(tc_path::tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_path::SMEM_BYTES);
+  // early row loads and L2 prefetch for a cache that does not stay in L2
+  auto kern = p.big_cache ? tc_path::tc_kernel<true> : tc_path::tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_path::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  tc_path::tc_kernel<<<(unsigned)grid, tc_path::NT, tc_path::SMEM_BYTES, stream>>>(p);
+  kern<<<(unsigned)grid, tc_path::NT, tc_path::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -169,6 +169,28 @@ def test_deterministic_repeat():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+# ----------------------------------------------------------------------------- caches beyond L2
+# A cache larger than a quarter of the device's L2 (at least 32 MB on GB300)
+# runs the tcgen05 kernel's early-load / L2-prefetch variant; these cases cover
+# it with the full oracle on every token.
+@pytest.mark.parametrize("H", [64, 128])
+def test_cache_beyond_l2_prefill(H):
+    wl = inputs.make_prefill("bigcache", T=5, H=H, ctx=65536, topk=704, seed=31, ragged=True, neg_prob=0.05)
+    assert wl.kv.numel() >= 40 << 20
+    out, lse = run_prefill(wl)
+    assert_close(out, lse, *oracle_for(wl), tag=f"bigcache_prefill_H{H}")
+    assert binding.get_error_word() == 0
+
+
+@pytest.mark.parametrize("S", [1, 3])
+def test_cache_beyond_l2_paged_decode(S):
+    wl = inputs.make_decode("bigcache_dec", n_req=4, tokens_per_req=2, H=64, ctx_per_req=16384, topk=1024, seed=37)
+    assert wl.kv.numel() >= 40 << 20
+    out, lse = run_decode(wl, num_splits=S)
+    assert_close(out, lse, *oracle_for(wl), tag=f"bigcache_decode_S{S}")
+    assert binding.get_error_word() == 0
+
+
 # ----------------------------------------------------------------------------- full-size workloads
 FULL = {
     "prefill16k_k512": (lambda: inputs.prefill_16k(512), "prefill", 48),
