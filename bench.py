@@ -54,21 +54,32 @@ def workloads(tokens=None):
                       parts=[("all", lambda s: inputs.large_prefill(seed=s, T=TL))]),
         "tiny": dict(name="tiny_prefill_T4_H8_ctx256_k64", kind="prefill", bound="hbm",
                      parts=[("all", lambda s: inputs.tiny_prefill(seed=s))]),
+        "dual_decode": dict(name="dual_decode_64req_x2_H64_ctx32768_k1024+ctx8192_k2176_paged", kind="dual_decode",
+                            bound="hbm", parts=[("all", lambda s: inputs.dual_decode(seed=s))]),
     }
 
 
-def valid_slots(wl):
-    """Number of valid (token, slot) pairs: the units the algorithmic work counts."""
+def _valid_in_list(indices, topk, topk_length, num_pages, block_table):
     import numpy as np
-    idx = wl.indices.numpy()[:, :wl.topk].astype(np.int64)
+    idx = indices.numpy()[:, :topk].astype(np.int64)
     T = idx.shape[0]
-    lens = np.full(T, wl.topk) if wl.topk_length is None else np.clip(wl.topk_length.numpy(), 0, wl.topk)
-    inlen = np.arange(wl.topk)[None, :] < lens[:, None]
-    if wl.block_table is None:
-        ok = inlen & (idx >= 0) & (idx < wl.num_pages * 64)
+    lens = np.full(T, topk) if topk_length is None else np.clip(topk_length.numpy(), 0, topk)
+    inlen = np.arange(topk)[None, :] < lens[:, None]
+    if block_table is None:
+        ok = inlen & (idx >= 0) & (idx < num_pages * 64)
     else:
-        ok = inlen & (idx >= 0) & (idx // 64 < wl.block_table.shape[1])
+        ok = inlen & (idx >= 0) & (idx // 64 < block_table.shape[1])
     return int(ok.sum())
+
+
+def valid_slots(wl):
+    """Number of valid (token, slot) pairs: the units the algorithmic work counts
+    (both lists of the dual-cache form)."""
+    v = _valid_in_list(wl.indices, wl.topk, wl.topk_length, wl.num_pages, wl.block_table)
+    if wl.dual:
+        v += _valid_in_list(wl.extra_indices, wl.extra_topk, wl.extra_topk_length, wl.extra_kv.shape[0],
+                            wl.extra_block_table)
+    return v
 
 
 def work_of(wl):
@@ -76,7 +87,7 @@ def work_of(wl):
     T, H = wl.T, wl.H
     flops = 2.0 * H * (576 + 512) * v
     gather = v * ROW
-    io = T * H * (576 * 2 + 512 * 2 + 4) + T * wl.topk * 4
+    io = T * H * (576 * 2 + 512 * 2 + 4) + T * (wl.topk + wl.extra_topk) * 4
     return dict(valid=v, flops=flops, bytes=gather + io, gather_bytes=gather)
 
 
@@ -94,9 +105,15 @@ def load_peaks():
 def _oracle_chunk(args):
     import numpy as np
     import oracle.sparse_mla_oracle as O
-    (q, kv, idx, topk, sm, tl, sink, bt, tpr, toks) = args
-    O.sparse_mla_forward(q, kv, idx, topk, sm, topk_length=tl, attn_sink=sink, block_table=bt,
-                         tokens_per_req=tpr, tokens=toks, q_selected=True)
+    (q, kv, idx, topk, sm, tl, sink, bt, tpr, toks, extra) = args
+    if extra is None:
+        O.sparse_mla_forward(q, kv, idx, topk, sm, topk_length=tl, attn_sink=sink, block_table=bt,
+                             tokens_per_req=tpr, tokens=toks, q_selected=True)
+    else:
+        kv2, idx2, topk2, tl2, bt2 = extra
+        O.sparse_mla_forward_dual(q, kv, idx, topk, kv2, idx2, topk2, sm, topk_length=tl, extra_topk_length=tl2,
+                                  attn_sink=sink, block_table=bt, extra_block_table=bt2, tokens_per_req=tpr,
+                                  tokens=toks, q_selected=True)
     return len(toks)
 
 
@@ -111,8 +128,11 @@ def oracle_time(wl, n_tokens, cores):
     tl = None if wl.topk_length is None else wl.topk_length.numpy()
     sink = None if wl.attn_sink is None else wl.attn_sink.numpy().astype(np.float64)
     bt = None if wl.block_table is None else wl.block_table.numpy()
+    np_ = lambda x: None if x is None else x.numpy()
+    extra = (wl.extra_kv.numpy(), wl.extra_indices.numpy(), wl.extra_topk, np_(wl.extra_topk_length),
+             np_(wl.extra_block_table)) if wl.dual else None
     jobs = [(wl.q[torch.as_tensor(c)].to(torch.float64).numpy(), kv, idx, wl.topk, wl.sm_scale, tl, sink, bt,
-             wl.tokens_per_req, c) for c in chunks]
+             wl.tokens_per_req, c, extra) for c in chunks]
     ctx = mp.get_context("spawn")
     with ctx.Pool(len(jobs), initializer=_pin_threads) as pool:
         pool.map(_oracle_chunk, jobs[:1])  # warm the workers' imports
@@ -216,12 +236,21 @@ def make_call(kind, binding, d, wl, out, lse, ws, num_splits):
                                        topk_length=d["topk_length"], attn_sink=d["attn_sink"],
                                        block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
                                        out=out, lse=lse, stream=stream)
-    else:
+    elif kind == "decode":
         def call(stream=None):
             binding.sparse_mla_decode(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
                                       topk_length=d["topk_length"], attn_sink=d["attn_sink"],
                                       block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
                                       num_splits=num_splits, workspace=ws, out=out, lse=lse, stream=stream)
+    else:
+        def call(stream=None):
+            binding.sparse_mla_decode_dual(d["q"], d["kv"], d["indices"], d["extra_kv"], d["extra_indices"],
+                                           wl.sm_scale, topk=wl.topk, topk_length=d["topk_length"],
+                                           extra_topk=wl.extra_topk, extra_topk_length=d["extra_topk_length"],
+                                           attn_sink=d["attn_sink"], block_table=d["block_table"],
+                                           extra_block_table=d["extra_block_table"],
+                                           tokens_per_req=wl.tokens_per_req, num_splits=num_splits, workspace=ws,
+                                           out=out, lse=lse, stream=stream)
     return call
 
 
@@ -238,18 +267,20 @@ def run_ours(args, rank, world, local_rank):
     for tag, mk in spec["parts"]:
         wl = mk(rank_seed(args.seed, rank))
         d = {k: (None if getattr(wl, k) is None else getattr(wl, k).to(dev))
-             for k in ("q", "kv", "indices", "topk_length", "attn_sink", "block_table")}
+             for k in ("q", "kv", "indices", "topk_length", "attn_sink", "block_table", "extra_kv",
+                       "extra_indices", "extra_topk_length", "extra_block_table")}
         out = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device=dev)
         ws = None
-        if spec["kind"] == "decode":
-            ws = torch.empty(max(256, binding.decode_workspace_size(wl.T, wl.H, wl.topk, args.num_splits)),
+        if spec["kind"] != "prefill":
+            width = binding.dual_width(wl.topk, wl.extra_topk) if wl.dual else wl.topk
+            ws = torch.empty(max(256, binding.decode_workspace_size(wl.T, wl.H, width, args.num_splits)),
                              dtype=torch.uint8, device=dev)
         call = make_call(spec["kind"], binding, d, wl, out, lse, ws, args.num_splits)
         parts.append(dict(tag=tag, wl=wl, d=d, out=out, lse=lse, ws=ws, call=call, work=work_of(wl)))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_part = 2 if spec["kind"] == "decode" else 1
+    launches_per_part = 1 if spec["kind"] == "prefill" else 2
 
     def barrier():
         if world > 1:
@@ -309,7 +340,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": spec["name"], "global_batch_tokens": tokens_per_step * world,
                    "parallelism": f"dp{world} (independent token shards, no collective)",
                    "l2": "flushed between steps (256 MiB write)", "seed": args.seed,
-                   "num_splits": args.num_splits if spec["kind"] == "decode" else None},
+                   "num_splits": args.num_splits if spec["kind"] != "prefill" else None},
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": args.steps * len(parts) * launches_per_part,
@@ -324,24 +355,24 @@ def run_e2e(args, parts, dev, stream, world):
     hosts = []
     for p in parts:
         wl = p["wl"]
-        hq = wl.q.pin_memory()
-        hi = wl.indices.pin_memory()
-        htl = None if wl.topk_length is None else wl.topk_length.pin_memory()
+        # per step: q and every index input travel host -> device
+        ins = [(wl.q.pin_memory(), "q")]
+        for k in ("indices", "topk_length", "extra_indices", "extra_topk_length"):
+            if getattr(wl, k) is not None:
+                ins.append((getattr(wl, k).pin_memory(), k))
         ho = torch.empty(p["out"].shape, dtype=p["out"].dtype).pin_memory()
         hl = torch.empty(p["lse"].shape, dtype=p["lse"].dtype).pin_memory()
-        hosts.append((hq, hi, htl, ho, hl))
+        hosts.append((ins, ho, hl))
     steps = max(1, min(args.steps, 20))
-    h2d = sum(h[0].numel() * 2 + h[1].numel() * 4 + (0 if h[2] is None else h[2].numel() * 4) for h in hosts)
-    d2h = sum(h[3].numel() * 2 + h[4].numel() * 4 for h in hosts)
+    h2d = sum(sum(t.numel() * t.element_size() for t, _ in h[0]) for h in hosts)
+    d2h = sum(h[1].numel() * 2 + h[2].numel() * 4 for h in hosts)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     start.record(stream)
     for _ in range(steps):
-        for p, (hq, hi, htl, ho, hl) in zip(parts, hosts):
-            p["d"]["q"].copy_(hq, non_blocking=True)
-            p["d"]["indices"].copy_(hi, non_blocking=True)
-            if htl is not None:
-                p["d"]["topk_length"].copy_(htl, non_blocking=True)
+        for p, (ins, ho, hl) in zip(parts, hosts):
+            for t, k in ins:
+                p["d"][k].copy_(t, non_blocking=True)
             p["call"]()
             ho.copy_(p["out"], non_blocking=True)
             hl.copy_(p["lse"], non_blocking=True)
@@ -401,7 +432,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["prefill16k", "fewhead", "decode", "large", "tiny"],
+    ap.add_argument("--workload", choices=["prefill16k", "fewhead", "decode", "large", "tiny", "dual_decode"],
                     default="prefill16k")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--seed", type=int, default=0)

@@ -209,6 +209,65 @@ int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags);
 #define SMLA_NOALLOC_SCRATCH_BYTES (64u << 20)
 int sparse_mla_decode_noalloc(const smla_args* args, int32_t num_splits, smla_stream_t stream);
 
+/*
+ * Dual-cache form: one softmax over the candidates of two index lists, each
+ * into its own cache (FlashInfer PR #4802: the "DSv4 secondary cache" whose
+ * index row stride comes from the tensor, the dual-cache decode-form calls
+ * that must not ignore the secondary cache, and the "topk=1024+2176 dual"
+ * decode shape).  args describes the first list and cache exactly as for
+ * sparse_mla_prefill / sparse_mla_decode; extra describes the second:
+ *
+ *  kv, num_pages   the second cache, same row format and page size.
+ *  block_table     int32 [bt_rows, >= bt_cols], row stride bt_stride, or
+ *                  NULL for flat row ids; shares args->tokens_per_req.
+ *  topk, indices, idx_stride_t, topk_length
+ *                  the second list, with the same slot rules as the first.
+ *
+ * For each token the result is the sink softmax of the Introduction over the
+ * union of both lists' valid slots (a row of each cache counts as many times
+ * as it is selected).  The lists are laid end to end as "combined slots": the
+ * first list padded with invalid slots to a multiple of 64, then the second,
+ * i.e. sparse_mla_dual_width(topk, extra->topk) slots per token.  Decode
+ * splits cut the combined slots into chunks of 64, so size its workspace as
+ *   sparse_mla_decode_workspace_size(T, H, sparse_mla_dual_width(topk,
+ *                                    extra->topk), num_splits).
+ * Readings where the pages are silent: the sink enters once per token (not
+ * once per list), and the second list's row ids are resolved in the second
+ * cache only.  Extra constraint: both caches together hold fewer than 2^31
+ * rows.  Error behaviour as for the single-list calls (SMLA_ERR_INVALID for
+ * a bad extra; out-of-range indices of either list set SMLA_ERRF_INDEX_RANGE).
+ */
+typedef struct smla_extra_args {
+  const uint8_t* kv;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int32_t bt_rows;
+  int32_t bt_cols;
+  int32_t topk;
+  int32_t reserved0; /* must be 0 */
+  const int32_t* indices;
+  int64_t idx_stride_t;
+  const int32_t* topk_length;
+} smla_extra_args;
+
+/* Combined slots per token of the dual-cache form (0 for invalid sizes). */
+int32_t sparse_mla_dual_width(int32_t topk, int32_t extra_topk);
+
+int sparse_mla_prefill_dual(const smla_args* args, const smla_extra_args* extra, smla_stream_t stream);
+
+int sparse_mla_decode_dual(const smla_args* args, const smla_extra_args* extra, int32_t num_splits,
+                           void* workspace, size_t workspace_bytes, smla_stream_t stream);
+
+/*
+ * Index handling of the dual-cache form: rows_out[t*rows_stride_t + s] for
+ * every combined slot s (rows_stride_t >= the combined width) receives the
+ * first cache's row for a first-list slot, args->num_pages*64 + the second
+ * cache's row for a second-list slot, or -1 for an invalid or padding slot.
+ */
+int sparse_mla_resolve_rows_dual(const smla_args* args, const smla_extra_args* extra, int32_t* rows_out,
+                                 int64_t rows_stride_t, smla_stream_t stream);
+
 /* Message for the last failing call on this thread ("" if none). */
 const char* sparse_mla_last_error(void);
 

@@ -50,7 +50,10 @@ example in ``tests/golden/``; dense attention via
 the whole context; the sink as an extra key through the same library routine;
 one valid index; identical rows; permutation invariance; paged == flat after a
 page shuffle; truncation == -1 padding; the split/merge algebra against the
-one-shot result.  Every function below has at least one of these pins.
+one-shot result; the dual-cache form against the one-list form (two caches
+stacked into one with the second list's ids shifted, an empty second list,
+the two lists swapped, and one list split in two over the same cache).  Every
+function below has at least one of these pins.
 """
 from __future__ import annotations
 
@@ -217,6 +220,44 @@ def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
     for i, t in enumerate(sel):
         r = rows[i]
         K = decode_rows(kv[r[r >= 0]])
+        out[i], lse[i] = attend_one(q[i] if q_selected else q[t], K, sm_scale, sink)
+    return out, lse
+
+
+def sparse_mla_forward_dual(q, kv_cache, indices, topk, extra_kv_cache, extra_indices, extra_topk,
+                            sm_scale, topk_length=None, extra_topk_length=None, attn_sink=None,
+                            block_table=None, extra_block_table=None, tokens_per_req=1,
+                            tokens=None, q_selected=False):
+    """Dual-cache form: one sink softmax per token over the valid slots of two
+    index lists, the first resolved in ``kv_cache`` and the second in
+    ``extra_kv_cache`` (FlashInfer PR #4802: the DSv4 secondary cache with its
+    own index row stride; dual-cache decode-form calls that must not ignore
+    the secondary cache; the "topk=1024+2176 dual" decode shape).
+
+    Each list follows the slot rules of ``resolve_rows`` in its own cache and
+    with its own ``topk`` / ``topk_length`` / block table (``tokens_per_req``
+    is shared).  The candidate set is the concatenation of both lists' valid
+    rows, and the sink enters the denominator once.
+    """
+    kv1 = np.asarray(kv_cache, dtype=np.uint8).reshape(-1, ROW_BYTES)
+    kv2 = np.asarray(extra_kv_cache, dtype=np.uint8).reshape(-1, ROW_BYTES)
+    q = np.asarray(q, dtype=np.float64)
+    T = np.asarray(indices).shape[0]
+    _, H, D = q.shape
+    assert D == D_QK and np.asarray(extra_indices).shape[0] == T
+    sel = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    if q_selected:
+        assert q.shape[0] == sel.shape[0]
+    rows1 = resolve_rows(indices, topk, kv1.shape[0] // PAGE_BLOCK, topk_length, block_table,
+                         tokens_per_req, sel)
+    rows2 = resolve_rows(extra_indices, extra_topk, kv2.shape[0] // PAGE_BLOCK, extra_topk_length,
+                         extra_block_table, tokens_per_req, sel)
+    out = np.zeros((sel.shape[0], H, D_V))
+    lse = np.zeros((sel.shape[0], H))
+    sink = None if attn_sink is None else np.asarray(attn_sink, dtype=np.float64)
+    for i, t in enumerate(sel):
+        r1, r2 = rows1[i], rows2[i]
+        K = np.concatenate([decode_rows(kv1[r1[r1 >= 0]]), decode_rows(kv2[r2[r2 >= 0]])], axis=0)
         out[i], lse[i] = attend_one(q[i] if q_selected else q[t], K, sm_scale, sink)
     return out, lse
 

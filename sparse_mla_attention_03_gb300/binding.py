@@ -46,8 +46,21 @@ class SmlaArgs(ctypes.Structure):
     ]
 
 
+class SmlaExtraArgs(ctypes.Structure):
+    """The second list and cache of the dual-cache form (``smla_extra_args``)."""
+    _fields_ = [
+        ("kv", ctypes.c_void_p), ("num_pages", ctypes.c_int64),
+        ("block_table", ctypes.c_void_p), ("bt_stride", ctypes.c_int64),
+        ("bt_rows", ctypes.c_int32), ("bt_cols", ctypes.c_int32),
+        ("topk", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("indices", ctypes.c_void_p), ("idx_stride_t", ctypes.c_int64),
+        ("topk_length", ctypes.c_void_p),
+    ]
+
+
 # (name, restype, argtypes) for every symbol of include/sparse_mla.h
 _P = ctypes.POINTER(SmlaArgs)
+_X = ctypes.POINTER(SmlaExtraArgs)
 SYMBOLS = {
     "sparse_mla_prefill": (ctypes.c_int, [_P, ctypes.c_void_p]),
     "sparse_mla_decode": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -58,6 +71,11 @@ SYMBOLS = {
     "sparse_mla_get_error_word": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "sparse_mla_last_error": (ctypes.c_char_p, []),
     "sparse_mla_abi_version": (ctypes.c_int32, []),
+    "sparse_mla_dual_width": (ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32]),
+    "sparse_mla_prefill_dual": (ctypes.c_int, [_P, _X, ctypes.c_void_p]),
+    "sparse_mla_decode_dual": (ctypes.c_int, [_P, _X, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
+                                              ctypes.c_void_p]),
+    "sparse_mla_resolve_rows_dual": (ctypes.c_int, [_P, _X, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
 }
 
 _lib = None
@@ -241,3 +259,98 @@ def get_error_word(stream=None) -> int:
     v = ctypes.c_int32(0)
     _check(load().sparse_mla_get_error_word(_stream_handle(stream), ctypes.byref(v)))
     return int(v.value)
+
+
+# ----------------------------------------------------------------------------- dual-cache form
+def make_extra(q, kv, indices, topk=None, topk_length=None, block_table=None) -> SmlaExtraArgs:
+    """Validate the second list / cache of the dual-cache form and build its struct."""
+    T = q.shape[0]
+    dev = q.device
+    topk = indices.shape[1] if topk is None else topk
+    for x, name, dtype in ((kv, "extra kv", torch.uint8), (indices, "extra indices", torch.int32),
+                           (topk_length, "extra topk_length", torch.int32),
+                           (block_table, "extra block_table", torch.int32)):
+        if x is None:
+            continue
+        if x.device != dev:
+            raise ValueError(f"{name} is on {x.device}, q is on {dev}")
+        if x.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {x.dtype}")
+    if kv.dim() != 3 or tuple(kv.shape[1:]) != (PAGE, ROW_BYTES) or not kv.is_contiguous():
+        raise ValueError("extra kv must be a contiguous [num_pages, 64, 656] uint8 tensor")
+    if indices.dim() != 2 or indices.shape[0] != T or indices.stride(1) != 1 or indices.shape[1] < topk:
+        raise ValueError("extra indices must be [T, >= topk] with a contiguous last dimension")
+    if topk_length is not None and (topk_length.shape != (T,) or topk_length.stride(0) != 1):
+        raise ValueError("extra topk_length must be a contiguous [T] tensor")
+    x = SmlaExtraArgs()
+    x.kv, x.num_pages = kv.data_ptr(), kv.shape[0]
+    if block_table is not None:
+        if block_table.dim() != 2 or block_table.stride(1) != 1:
+            raise ValueError("extra block_table must be [B, max_pages] with a contiguous last dimension")
+        x.block_table = block_table.data_ptr()
+        x.bt_stride = block_table.stride(0)
+        x.bt_rows, x.bt_cols = block_table.shape
+    x.topk = int(topk)
+    x.indices, x.idx_stride_t = indices.data_ptr(), indices.stride(0)
+    x.topk_length = _ptr(topk_length)
+    return x
+
+
+def dual_width(topk, extra_topk) -> int:
+    """Combined slots per token of the dual-cache form."""
+    return int(load().sparse_mla_dual_width(int(topk), int(extra_topk)))
+
+
+def sparse_mla_prefill_dual(q, kv, indices, extra_kv, extra_indices, sm_scale, topk=None, topk_length=None,
+                            extra_topk=None, extra_topk_length=None, attn_sink=None, block_table=None,
+                            extra_block_table=None, tokens_per_req=1, out=None, lse=None, stream=None):
+    """One softmax over two index lists into two caches; returns ``(out, lse)``."""
+    lib = load()
+    topk = indices.shape[1] if topk is None else topk
+    out, lse = _outputs(q, out, lse)
+    a = make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length, attn_sink, block_table,
+                  tokens_per_req)
+    a.tokens_per_req = int(tokens_per_req)
+    x = make_extra(q, extra_kv, extra_indices, extra_topk, extra_topk_length, extra_block_table)
+    _check(lib.sparse_mla_prefill_dual(ctypes.byref(a), ctypes.byref(x), _stream_handle(stream)))
+    return out, lse
+
+
+def sparse_mla_decode_dual(q, kv, indices, extra_kv, extra_indices, sm_scale, topk=None, topk_length=None,
+                           extra_topk=None, extra_topk_length=None, attn_sink=None, block_table=None,
+                           extra_block_table=None, tokens_per_req=1, num_splits=0, workspace=None,
+                           out=None, lse=None, stream=None):
+    """Split-K decode of the dual-cache form plus combine; returns ``(out, lse)``."""
+    lib = load()
+    topk = indices.shape[1] if topk is None else topk
+    out, lse = _outputs(q, out, lse)
+    a = make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length, attn_sink, block_table,
+                  tokens_per_req)
+    a.tokens_per_req = int(tokens_per_req)
+    x = make_extra(q, extra_kv, extra_indices, extra_topk, extra_topk_length, extra_block_table)
+    need = decode_workspace_size(q.shape[0], q.shape[1], dual_width(topk, x.topk), num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(lib.sparse_mla_decode_dual(ctypes.byref(a), ctypes.byref(x), int(num_splits), workspace.data_ptr(),
+                                      workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+    return out, lse
+
+
+def sparse_mla_resolve_rows_dual(q, kv, indices, extra_kv, extra_indices, topk=None, topk_length=None,
+                                 extra_topk=None, extra_topk_length=None, block_table=None,
+                                 extra_block_table=None, tokens_per_req=1, stream=None):
+    """Row per combined slot (int32 [T, width]); second-cache rows are offset
+    by the first cache's row count; -1 = invalid or padding."""
+    lib = load()
+    topk = indices.shape[1] if topk is None else topk
+    T, H = q.shape[0], q.shape[1]
+    out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    a = make_args(q, kv, indices, topk, 1.0, out, lse, topk_length, None, block_table, tokens_per_req)
+    a.tokens_per_req = int(tokens_per_req)
+    x = make_extra(q, extra_kv, extra_indices, extra_topk, extra_topk_length, extra_block_table)
+    width = dual_width(topk, x.topk)
+    rows = torch.empty((T, width), dtype=torch.int32, device=q.device)
+    _check(lib.sparse_mla_resolve_rows_dual(ctypes.byref(a), ctypes.byref(x), rows.data_ptr(), width,
+                                            _stream_handle(stream)))
+    return rows

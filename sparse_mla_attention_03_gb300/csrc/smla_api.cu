@@ -125,6 +125,64 @@ smla::KParams make_params(const smla_args* a, int dev) {
   // meet with L2 prefetch and earlier register loads.
   p.big_cache = (int64_t)a->num_pages * SMLA_PAGE * SMLA_ROW_BYTES > g_l2_bytes[dev] / 4 ? 1 : 0;
   p.err = g_err_ptr[dev];
+  // one list: the second-list fields stay inert
+  p.dual = 0;
+  p.x_base = 0x7FFFFFFF;
+  p.rows1 = (int32_t)(a->num_pages * SMLA_PAGE);
+  p.topk2 = 0;
+  return p;
+}
+
+// Combined slot width of the dual-cache form: the first list padded to whole
+// 64-slot chunks, then the second list.
+int64_t dual_width(int64_t topk, int64_t topk2) { return ((topk + 63) / 64) * 64 + topk2; }
+
+int validate_extra(const smla_args* a, const smla_extra_args* x) {
+  if (x == nullptr) return fail(SMLA_ERR_INVALID, "extra is NULL");
+  if (x->reserved0 != 0) return fail(SMLA_ERR_INVALID, "extra->reserved0 must be 0");
+  if (x->topk < 1) return fail(SMLA_ERR_INVALID, "extra->topk = %d < 1", x->topk);
+  if (dual_width(a->topk, x->topk) > (1 << 24))
+    return fail(SMLA_ERR_INVALID, "combined slot width %lld too large", (long long)dual_width(a->topk, x->topk));
+  if (a->T == 0) return SMLA_OK;
+  if (!x->indices) return fail(SMLA_ERR_INVALID, "extra->indices is NULL");
+  if (x->idx_stride_t < x->topk) return fail(SMLA_ERR_INVALID, "extra->idx_stride_t < extra->topk");
+  if (x->num_pages < 0 || x->num_pages * SMLA_PAGE > 0x7FFFFFFFLL)
+    return fail(SMLA_ERR_INVALID, "extra->num_pages = %lld out of range", (long long)x->num_pages);
+  if ((a->num_pages + x->num_pages) * SMLA_PAGE > 0x7FFFFFFFLL)
+    return fail(SMLA_ERR_INVALID, "the two caches hold more than 2^31 - 1 rows together");
+  if (x->num_pages > 0 && !x->kv) return fail(SMLA_ERR_INVALID, "extra->kv is NULL");
+  if (x->kv && !aligned(x->kv, 16)) return fail(SMLA_ERR_INVALID, "extra->kv must be 16-byte aligned");
+  if (!aligned(x->indices, 4)) return fail(SMLA_ERR_INVALID, "misaligned extra->indices");
+  if (x->topk_length && !aligned(x->topk_length, 4)) return fail(SMLA_ERR_INVALID, "misaligned extra->topk_length");
+  if (x->block_table) {
+    if (a->tokens_per_req < 1) return fail(SMLA_ERR_INVALID, "tokens_per_req < 1");
+    if (x->bt_cols < 1 || x->bt_stride < x->bt_cols || x->bt_rows < 1)
+      return fail(SMLA_ERR_INVALID, "bad extra block table shape (rows %d, cols %d, stride %lld)", x->bt_rows,
+                  x->bt_cols, (long long)x->bt_stride);
+    if ((int64_t)x->bt_rows * a->tokens_per_req < a->T)
+      return fail(SMLA_ERR_INVALID, "extra block table has %d rows for %d tokens at %d tokens/request",
+                  x->bt_rows, a->T, a->tokens_per_req);
+    if (!aligned(x->block_table, 4)) return fail(SMLA_ERR_INVALID, "misaligned extra->block_table");
+  }
+  return SMLA_OK;
+}
+
+smla::KParams make_params_dual(const smla_args* a, const smla_extra_args* x, int dev) {
+  smla::KParams p = make_params(a, dev);
+  p.dual = 1;
+  p.x_base = (int32_t)(((a->topk + 63) / 64) * 64);
+  p.topk2 = x->topk;
+  p.kv2 = x->kv;
+  p.num_pages2 = x->num_pages;
+  p.block_table2 = x->block_table;
+  p.bt2_stride = x->bt_stride;
+  p.bt2_cols = x->bt_cols;
+  p.indices2 = x->indices;
+  p.idx2_stride_t = x->idx_stride_t;
+  p.topk_length2 = x->topk_length;
+  if (x->block_table) p.tokens_per_req = a->tokens_per_req;
+  p.split_len = (int32_t)(((dual_width(a->topk, x->topk) + 63) / 64) * 64);
+  p.big_cache = (a->num_pages + x->num_pages) * SMLA_PAGE * SMLA_ROW_BYTES > g_l2_bytes[dev] / 4 ? 1 : 0;
   return p;
 }
 
@@ -174,11 +232,34 @@ size_t ws_bytes(int64_t T, int64_t H, int64_t S) {
   return ((o + 255) / 256) * 256 + ((l + 255) / 256) * 256;
 }
 
+// Split launch plus combine over a slot width of `width` (topk, or the
+// combined width of the dual-cache form).
+int decode_launch(smla::KParams p, int width, int num_splits, void* workspace, size_t workspace_bytes,
+                  smla_stream_t stream, int dev) {
+  const int S = splits_for(p.T, p.H, width, num_splits, g_num_sms[dev]);
+  const size_t need = ws_bytes(p.T, p.H, S);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(SMLA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+  if (!aligned(workspace, 256)) return fail(SMLA_ERR_INVALID, "workspace must be 256-byte aligned");
+  const int chunks = (width + 63) / 64;
+  p.num_splits = S;
+  p.split_len = ((chunks + S - 1) / S) * 64;
+  const size_t o_bytes = (size_t)p.T * p.H * S * SMLA_D_V * sizeof(float);
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = smla::launch_attention(p, st);
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode split launch: %s", cudaGetErrorString(e));
+  e = smla::launch_combine(p, st);
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode combine launch: %s", cudaGetErrorString(e));
+  return SMLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-int32_t sparse_mla_abi_version(void) { return 1; }
+int32_t sparse_mla_abi_version(void) { return 2; }
 
 const char* sparse_mla_last_error(void) { return g_last_error; }
 
@@ -223,24 +304,41 @@ int sparse_mla_decode(const smla_args* a, int32_t num_splits, void* workspace, s
   if (a->T == 0) return SMLA_OK;  // zero tokens: nothing to launch
   int dev;
   if ((rc = device_setup(&dev)) != SMLA_OK) return rc;
-  const int S = splits_for(a->T, a->H, a->topk, num_splits, g_num_sms[dev]);
-  const size_t need = ws_bytes(a->T, a->H, S);
-  if (workspace == nullptr || workspace_bytes < need)
-    return fail(SMLA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
-  if (!aligned(workspace, 256)) return fail(SMLA_ERR_INVALID, "workspace must be 256-byte aligned");
-  smla::KParams p = make_params(a, dev);
-  const int chunks = (a->topk + 63) / 64;
-  p.num_splits = S;
-  p.split_len = ((chunks + S - 1) / S) * 64;
-  const size_t o_bytes = (size_t)a->T * a->H * S * SMLA_D_V * sizeof(float);
-  p.ws_o = static_cast<float*>(workspace);
-  p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = smla::launch_attention(p, st);
-  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode split launch: %s", cudaGetErrorString(e));
-  e = smla::launch_combine(p, st);
-  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode combine launch: %s", cudaGetErrorString(e));
+  return decode_launch(make_params(a, dev), a->topk, num_splits, workspace, workspace_bytes, stream, dev);
+}
+
+int32_t sparse_mla_dual_width(int32_t topk, int32_t extra_topk) {
+  if (topk < 1 || extra_topk < 1 || dual_width(topk, extra_topk) > (1 << 24)) return 0;
+  return (int32_t)dual_width(topk, extra_topk);
+}
+
+int sparse_mla_prefill_dual(const smla_args* a, const smla_extra_args* x, smla_stream_t stream) {
+  g_last_error[0] = 0;
+  int rc = validate(a);
+  if (rc != SMLA_OK) return rc;
+  if ((rc = validate_extra(a, x)) != SMLA_OK) return rc;
+  if (a->T == 0) return SMLA_OK;
+  int dev;
+  if ((rc = device_setup(&dev)) != SMLA_OK) return rc;
+  smla::KParams p = make_params_dual(a, x, dev);
+  cudaError_t e = smla::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "dual prefill launch: %s", cudaGetErrorString(e));
   return SMLA_OK;
+}
+
+int sparse_mla_decode_dual(const smla_args* a, const smla_extra_args* x, int32_t num_splits, void* workspace,
+                           size_t workspace_bytes, smla_stream_t stream) {
+  g_last_error[0] = 0;
+  int rc = validate(a);
+  if (rc != SMLA_OK) return rc;
+  if ((rc = validate_extra(a, x)) != SMLA_OK) return rc;
+  if (num_splits < 0 || num_splits > SMLA_MAX_SPLITS)
+    return fail(SMLA_ERR_INVALID, "num_splits = %d not in [0, 64]", num_splits);
+  if (a->T == 0) return SMLA_OK;
+  int dev;
+  if ((rc = device_setup(&dev)) != SMLA_OK) return rc;
+  return decode_launch(make_params_dual(a, x, dev), (int)dual_width(a->topk, x->topk), num_splits, workspace,
+                       workspace_bytes, stream, dev);
 }
 
 int sparse_mla_resolve_rows(const smla_args* a, int32_t* rows_out, int64_t rows_stride_t, smla_stream_t stream) {
@@ -253,6 +351,24 @@ int sparse_mla_resolve_rows(const smla_args* a, int32_t* rows_out, int64_t rows_
   int dev;
   if ((rc = device_setup(&dev)) != SMLA_OK) return rc;
   smla::KParams p = make_params(a, dev);
+  cudaError_t e = smla::launch_resolve(p, rows_out, rows_stride_t, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "resolve launch: %s", cudaGetErrorString(e));
+  return SMLA_OK;
+}
+
+int sparse_mla_resolve_rows_dual(const smla_args* a, const smla_extra_args* x, int32_t* rows_out,
+                                 int64_t rows_stride_t, smla_stream_t stream) {
+  g_last_error[0] = 0;
+  int rc = validate(a);
+  if (rc != SMLA_OK) return rc;
+  if ((rc = validate_extra(a, x)) != SMLA_OK) return rc;
+  if (a->T == 0) return SMLA_OK;
+  const int64_t width = dual_width(a->topk, x->topk);
+  if (rows_out == nullptr || rows_stride_t < width)
+    return fail(SMLA_ERR_INVALID, "rows_out is NULL or rows_stride_t < the combined width %lld", (long long)width);
+  int dev;
+  if ((rc = device_setup(&dev)) != SMLA_OK) return rc;
+  smla::KParams p = make_params_dual(a, x, dev);
   cudaError_t e = smla::launch_resolve(p, rows_out, rows_stride_t, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "resolve launch: %s", cudaGetErrorString(e));
   return SMLA_OK;

@@ -71,22 +71,28 @@ cudaError_t launch_combine(const KParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// rows[t * rows_stride + j] = physical row of slot j of token t, or -1.
-__global__ void resolve_kernel(const KParams p, int32_t* rows, int64_t rows_stride) {
+// rows[t * rows_stride + s] = cache row of combined slot s of token t, or -1
+// (second-list rows of the dual-cache form are encoded as rows1 + row).  The
+// same slot routines as the attention kernels, with the dual-capable
+// instantiation, which also serves one list (x_base INT32_MAX, topk2 0).
+__global__ void resolve_kernel(const KParams p, int width, int32_t* rows, int64_t rows_stride) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (int64_t)p.T * p.topk) return;
-  const int t = (int)(i / p.topk), j = (int)(i % p.topk);
+  if (i >= (int64_t)p.T * width) return;
+  const int t = (int)(i / width), s = (int)(i % width);
+  const TokSlots ts = token_slots<true>(p, t);
   int r = -1;
-  if (j < token_len(p, t)) r = resolve_row(p, bt_row_of(p, t), __ldg(p.indices + (int64_t)t * p.idx_stride_t + j));
-  rows[(int64_t)t * rows_stride + j] = r;
+  if (s < ts.end && slot_readable<true>(p, s, ts.len1))
+    r = resolve_slot<true>(p, bt_row_of(p, t), bt2_row_of(p, t), s, slot_index<true>(p, t, s));
+  rows[(int64_t)t * rows_stride + s] = r;
 }
 
 cudaError_t launch_resolve(const KParams& p, int32_t* rows, int64_t rows_stride, cudaStream_t stream) {
-  const int64_t n = (int64_t)p.T * p.topk;
+  const int width = p.dual ? p.x_base + p.topk2 : p.topk;
+  const int64_t n = (int64_t)p.T * width;
   const int64_t blocks = (n + 255) / 256;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  resolve_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, rows, rows_stride);
+  resolve_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, width, rows, rows_stride);
   return cudaGetLastError();
 }
 

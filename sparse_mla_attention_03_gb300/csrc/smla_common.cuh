@@ -62,6 +62,22 @@ struct KParams {
   float* ws_o;        // [T, H, S, 512] fp32 partial outputs (normalised, sink-free)
   float* ws_lse;      // [T, H, S] fp32 partial LSE (natural log)
   int32_t big_cache;   // 1: cache larger than a quarter of L2 (its rows mostly come from HBM)
+  // Dual-cache form: a second list of slots into a second cache follows the
+  // first list, whose width is padded to a multiple of 64 slots.  Unused
+  // (dual 0, x_base INT32_MAX, topk2 0) for one list.
+  int32_t dual;
+  int32_t x_base;              // first combined slot of the second list
+  int32_t rows1;               // num_pages * 64: second-cache rows are encoded as rows1 + row
+  int32_t topk2;
+  const uint8_t* kv2;
+  int64_t num_pages2;
+  const int32_t* block_table2;  // nullptr: flat row ids
+  int64_t bt2_stride;
+  int32_t bt2_cols;
+  int32_t reserved_;
+  const int32_t* indices2;
+  int64_t idx2_stride_t;
+  const int32_t* topk_length2;  // nullptr: topk2
   int* err;           // device error word
 };
 
@@ -78,35 +94,104 @@ __device__ __forceinline__ int token_len(const KParams& p, int t) {
   return l < 0 ? 0 : (l > p.topk ? p.topk : l);
 }
 
-__device__ __forceinline__ int resolve_row(const KParams& p, const int32_t* bt_row, int idx) {
+// Row of index idx in a cache of num_pages pages (flat when bt_row is null).
+__device__ __forceinline__ int resolve_in(int64_t num_pages, const int32_t* bt_row, int bt_cols, int idx, int* err) {
   if (idx < 0) {
-    if (idx != -1) atomicOr(p.err, kErrIndexRange);
+    if (idx != -1) atomicOr(err, kErrIndexRange);
     return -1;
   }
   if (bt_row == nullptr) {
-    if ((int64_t)idx >= p.num_pages * kPage) {
-      atomicOr(p.err, kErrIndexRange);
+    if ((int64_t)idx >= num_pages * kPage) {
+      atomicOr(err, kErrIndexRange);
       return -1;
     }
     return idx;
   }
   const int lp = idx >> 6;
-  if (lp >= p.bt_cols) {
-    atomicOr(p.err, kErrIndexRange);
+  if (lp >= bt_cols) {
+    atomicOr(err, kErrIndexRange);
     return -1;
   }
   const int pp = __ldg(bt_row + lp);
-  if (pp < 0 || (int64_t)pp >= p.num_pages) {
-    atomicOr(p.err, kErrIndexRange);
+  if (pp < 0 || (int64_t)pp >= num_pages) {
+    atomicOr(err, kErrIndexRange);
     return -1;
   }
   return pp * kPage + (idx & (kPage - 1));
+}
+
+__device__ __forceinline__ int resolve_row(const KParams& p, const int32_t* bt_row, int idx) {
+  return resolve_in(p.num_pages, bt_row, p.bt_cols, idx, p.err);
 }
 
 __device__ __forceinline__ const int32_t* bt_row_of(const KParams& p, int t) {
   return p.block_table == nullptr
              ? nullptr
              : p.block_table + (int64_t)(t / p.tokens_per_req) * p.bt_stride;
+}
+
+// ---------------------------------------------------------------------------
+// Combined slots.  With one list, slot s of token t is slot s of its index
+// row.  In the dual-cache form (kDual, p.dual) slots [0, x_base) are the first
+// list (valid only below its topk_length) and slots [x_base, x_base + topk2)
+// the second list, resolved in the second cache and encoded as rows1 + row.
+// All candidates of a token enter one softmax.  kDual == false compiles the
+// single-list path with no trace of the second list.
+// ---------------------------------------------------------------------------
+struct TokSlots {
+  int len1;  // first-list entries at or past len1 are not read
+  int end;   // slots [0, end) may hold valid candidates
+};
+
+template <bool kDual>
+__device__ __forceinline__ TokSlots token_slots(const KParams& p, int t) {
+  const int l1 = token_len(p, t);
+  if (!kDual) return {l1, l1};
+  int l2 = p.topk2;
+  if (p.topk_length2 != nullptr) {
+    const int l = __ldg(p.topk_length2 + t);
+    l2 = l < 0 ? 0 : (l > p.topk2 ? p.topk2 : l);
+  }
+  return {l1, l2 > 0 ? p.x_base + l2 : l1};
+}
+
+template <bool kDual>
+__device__ __forceinline__ bool in_list2(const KParams& p, int s) {
+  return kDual && s >= p.x_base;
+}
+
+// Whether slot s's index entry may be read (the caller checks s < end).
+template <bool kDual>
+__device__ __forceinline__ bool slot_readable(const KParams& p, int s, int len1) {
+  return s < len1 || in_list2<kDual>(p, s);
+}
+
+template <bool kDual>
+__device__ __forceinline__ int slot_index(const KParams& p, int t, int s) {
+  if (in_list2<kDual>(p, s)) return __ldg(p.indices2 + (int64_t)t * p.idx2_stride_t + (s - p.x_base));
+  return __ldg(p.indices + (int64_t)t * p.idx_stride_t + s);
+}
+
+__device__ __forceinline__ const int32_t* bt2_row_of(const KParams& p, int t) {
+  return p.block_table2 == nullptr
+             ? nullptr
+             : p.block_table2 + (int64_t)(t / p.tokens_per_req) * p.bt2_stride;
+}
+
+// Row of slot s with index idx (-1: invalid), given the token's block-table
+// rows of both lists.
+template <bool kDual>
+__device__ __forceinline__ int resolve_slot(const KParams& p, const int32_t* btr, const int32_t* btr2, int s,
+                                            int idx) {
+  if (!in_list2<kDual>(p, s)) return resolve_row(p, btr, idx);
+  const int r = resolve_in(p.num_pages2, btr2, p.bt2_cols, idx, p.err);
+  return r < 0 ? -1 : p.rows1 + r;
+}
+
+template <bool kDual>
+__device__ __forceinline__ const uint8_t* row_ptr(const KParams& p, int r) {
+  if (kDual && r >= p.rows1) return p.kv2 + (int64_t)(r - p.rows1) * kRowBytes;
+  return p.kv + (int64_t)r * kRowBytes;
 }
 
 // ---------------------------------------------------------------------------

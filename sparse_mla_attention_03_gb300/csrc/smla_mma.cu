@@ -63,7 +63,7 @@ __device__ __forceinline__ uint32_t wsel(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
-template <int NH8, int NST>
+template <int NH8, int NST, bool kDual>
 __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams p) {
   constexpr int HG = NH8 * 8;
   using L = Layout<NH8, NST>;
@@ -79,12 +79,12 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
   const int t = bid / n_hg;
   const int h0 = hg * HG;
 
-  const int len = token_len(p, t);
+  const TokSlots ts = token_slots<kDual>(p, t);
   const int lo = split * p.split_len;
-  const int hi = min(len, lo + p.split_len);
+  const int hi = min(ts.end, lo + p.split_len);
   const int ntiles = hi > lo ? (hi - lo + BC - 1) / BC : 0;
-  const int32_t* idx_row = p.indices + (int64_t)t * p.idx_stride_t;
   const int32_t* btr = bt_row_of(p, t);
+  const int32_t* btr2 = kDual ? bt2_row_of(p, t) : nullptr;
 
   float* s_red = reinterpret_cast<float*>(smem + L::red);
   float* s_lsum = reinterpret_cast<float*>(smem + L::lsum);
@@ -129,7 +129,8 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
   auto issue = [&](int tile, int stage) -> uint32_t {
     const int slot = lo + tile * BC + warp * 16 + (lane & 15);
     int row = -1;
-    if (lane < 16 && slot < hi) row = resolve_row(p, btr, __ldg(idx_row + slot));
+    if (lane < 16 && slot < hi && slot_readable<kDual>(p, slot, ts.len1))
+      row = resolve_slot<kDual>(p, btr, btr2, slot, slot_index<kDual>(p, t, slot));
     uint8_t* base = smem + L::kv + stage * BC * TS + warp * 16 * TS;
 #pragma unroll 3
     for (int i = 0; i < 21; ++i) {
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
       const int rr = __shfl_sync(0xffffffffu, row, r & 15);
       if (f < 16 * 41) {
         const uint32_t dst = smem_u32(base + r * TS + swz(warp * 16 + r, ch) * 16);
-        const uint8_t* src = rr >= 0 ? p.kv + (int64_t)rr * kRowBytes + ch * 16 : p.kv;
+        const uint8_t* src = rr >= 0 ? row_ptr<kDual>(p, rr) + ch * 16 : p.kv;
         cp_async16(dst, src, rr >= 0 ? 16 : 0);
       }
     }
@@ -414,16 +415,17 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
   }
 }
 
-template <int NH8, int NST>
+template <int NH8, int NST, bool kDual>
 static cudaError_t launch(const KParams& p, cudaStream_t stream) {
   using L = Layout<NH8, NST>;
   const int n_hg = (p.H + NH8 * 8 - 1) / (NH8 * 8);
   const int64_t grid = (int64_t)p.T * n_hg * p.num_splits;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(mma_kernel<NH8, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
+  cudaError_t e =
+      cudaFuncSetAttribute(mma_kernel<NH8, NST, kDual>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
   if (e != cudaSuccess) return e;
-  mma_kernel<NH8, NST><<<(unsigned)grid, NT, L::total, stream>>>(p);
+  mma_kernel<NH8, NST, kDual><<<(unsigned)grid, NT, L::total, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -432,7 +434,11 @@ static cudaError_t launch(const KParams& p, cudaStream_t stream) {
 int mma_heads_per_cta(int H) { return H <= 8 ? 8 : 16; }
 
 cudaError_t launch_mma(const KParams& p, cudaStream_t stream) {
-  return mma_heads_per_cta(p.H) == 8 ? mma_path::launch<1, 1>(p, stream) : mma_path::launch<2, 2>(p, stream);
+  if (p.dual)
+    return mma_heads_per_cta(p.H) == 8 ? mma_path::launch<1, 1, true>(p, stream)
+                                       : mma_path::launch<2, 2, true>(p, stream);
+  return mma_heads_per_cta(p.H) == 8 ? mma_path::launch<1, 1, false>(p, stream)
+                                     : mma_path::launch<2, 2, false>(p, stream);
 }
 
 }  // namespace smla

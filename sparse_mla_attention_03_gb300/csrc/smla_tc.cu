@@ -400,11 +400,12 @@ __device__ __forceinline__ void xreduce64(const float (&x)[64], float& r0, float
 // coalesced (4 lanes read 64 contiguous bytes of one row), and the 16 rows'
 // scale and rope chunks (9 per row) are read as 144 consecutive (row, chunk)
 // pairs.
-template <bool kEarly>
+template <bool kEarly, bool kDual>
 __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32_t sbase, uint32_t bars, int t,
-                                         int lo, int hi, int ntiles, int pw, int lane, volatile int* s_abort) {
-  const int32_t* idx_row = p.indices + (int64_t)t * p.idx_stride_t;
+                                         int len1, int lo, int hi, int ntiles, int pw, int lane,
+                                         volatile int* s_abort) {
   const int32_t* btr = bt_row_of(p, t);
+  const int32_t* btr2 = kDual ? bt2_row_of(p, t) : nullptr;
   float* s_sc = reinterpret_cast<float*>(smem + OFF_SCALE) + pw * 64;  // [16 rows][4]
   // nope[g][j]: lane l holds row 8(j/2) + 2(l/8) + (l/4)%2, chunk 8g + 4(j%2) + l%4.
   // Each 8-lane store phase then covers two adjacent rows, whose different
@@ -414,7 +415,9 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
   // index reads (lanes 0..15: one row each)
   auto load_idx = [&](int it) -> int {
     const int slot = lo + it * BM + 16 * pw + lane;
-    return (lane < 16 && it < ntiles && slot < hi) ? __ldg(idx_row + slot) : -1;
+    return (lane < 16 && it < ntiles && slot < hi && slot_readable<kDual>(p, slot, len1))
+               ? slot_index<kDual>(p, t, slot)
+               : -1;
   };
   // Slot indices are read two tiles ahead of the conversion.  With rows that
   // stay in L2 (!kEarly), the next tile is loaded into registers in one burst
@@ -435,11 +438,11 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
     idx_b = load_idx(it + 2);
     if (lane < 16) {
       const int slot = lo + it * BM + 16 * pw + lane;
-      if (slot < hi) rowid = resolve_row(p, btr, idx);
+      if (slot < hi) rowid = resolve_slot<kDual>(p, btr, btr2, slot, idx);
       if (kEarly && it + 1 < ntiles && slot + BM < hi) {
-        const int r1 = resolve_row(p, btr, idx1);
+        const int r1 = resolve_slot<kDual>(p, btr, btr2, slot + BM, idx1);
         if (r1 >= 0)
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.kv + (int64_t)r1 * kRowBytes),
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row_ptr<kDual>(p, r1)),
                        "r"(kRowBytes)
                        : "memory");
       }
@@ -451,7 +454,7 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int r = __shfl_sync(0xffffffffu, rowid, 8 * (j >> 1) + 2 * (lane >> 3) + ((lane >> 2) & 1));
-      const uint4* src = reinterpret_cast<const uint4*>(p.kv + (int64_t)(r < 0 ? 0 : r) * kRowBytes);
+      const uint4* src = reinterpret_cast<const uint4*>(row_ptr<kDual>(p, r < 0 ? 0 : r));
       nope[g][j] = r >= 0 ? __ldg(src + 8 * g + 4 * (j & 1) + (lane & 3)) : z;
     }
   };
@@ -461,7 +464,7 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
       const int f = 32 * k + lane;
       const int rr = f < 144 ? f / 9 : 0;
       const int r = __shfl_sync(0xffffffffu, rowid, rr);
-      const uint4* src = reinterpret_cast<const uint4*>(p.kv + (int64_t)(r < 0 ? 0 : r) * kRowBytes);
+      const uint4* src = reinterpret_cast<const uint4*>(row_ptr<kDual>(p, r < 0 ? 0 : r));
       tail[k] = (f < 144 && r >= 0) ? __ldg(src + 32 + (f - 9 * rr)) : z;
     }
   };
@@ -547,7 +550,7 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
   }
 }
 
-template <bool kEarly>
+template <bool kEarly, bool kDual>
 __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the __shared__ array so
@@ -563,9 +566,9 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   const int hg = bid % n_hg;
   const int t = bid / n_hg;
   const int h0 = hg * HG;
-  const int len = token_len(p, t);
+  const TokSlots ts = token_slots<kDual>(p, t);
   const int lo = split * p.split_len;
-  const int hi = min(len, lo + p.split_len);
+  const int hi = min(ts.end, lo + p.split_len);
   const int ntiles = hi > lo ? (hi - lo + BM - 1) / BM : 0;
 
   float* s_qmul = reinterpret_cast<float*>(smem + OFF_QMUL);
@@ -608,7 +611,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   if (warp < W_SOFT) {
     // ============================================================ producers
     asm volatile("setmaxnreg.inc.sync.aligned.u32 136;" ::: "memory");
-    producer<kEarly>(p, smem, sbase, bars, t, lo, hi, ntiles, warp, lane, s_abort);
+    producer<kEarly, kDual>(p, smem, sbase, bars, t, ts.len1, lo, hi, ntiles, warp, lane, s_abort);
   } else if (warp >= W_MMA) {
     // ============================================================ MMA issue (warp 12; 13-15 idle)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
@@ -760,19 +763,22 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     float lsum0 = 0.f, lsum1 = 0.f;
     bool alive = true;
     bool refs_set = false;  // uniform: every head has a finite reference max
-    const int32_t* idx_row = p.indices + (int64_t)t * p.idx_stride_t;
     const int32_t* btr = bt_row_of(p, t);
+    const int32_t* btr2 = kDual ? bt2_row_of(p, t) : nullptr;
+    auto index_at = [&](int sl) -> int {  // -1 past the token's slots
+      return (sl < hi && slot_readable<kDual>(p, sl, ts.len1)) ? slot_index<kDual>(p, t, sl) : -1;
+    };
     // the slot index of tile it+1 is read during tile it and resolved at its
     // end, off the softmax's critical path
     bool valid_next = false;
-    if (ntiles > 0 && lo + c < hi) valid_next = resolve_row(p, btr, __ldg(idx_row + lo + c)) >= 0;
-    int idx_ahead = (ntiles > 1 && lo + BM + c < hi) ? __ldg(idx_row + lo + BM + c) : -1;
+    if (ntiles > 0) valid_next = resolve_slot<kDual>(p, btr, btr2, lo + c, index_at(lo + c)) >= 0;
+    int idx_ahead = ntiles > 1 ? index_at(lo + BM + c) : -1;
     for (int it = 0; it < ntiles; ++it) {
       const int slot = lo + it * BM + c;
       const bool valid = valid_next;
       const int idx1 = idx_ahead;
       const int slot2 = slot + 2 * BM;
-      idx_ahead = (it + 2 < ntiles && slot2 < hi) ? __ldg(idx_row + slot2) : -1;
+      idx_ahead = it + 2 < ntiles ? index_at(slot2) : -1;
       const bool failed = !mbar_wait(bar(B_SFULL), it & 1, s_abort, p.err);
       if (bar_or(1, 128, failed)) {
         alive = false;
@@ -873,7 +879,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       mbar_arrive(bar(B_PFULL));
       lsum0 += xreduce32_at<false, 0>(x);
       lsum1 += xreduce32_at<false, 32>(x);
-      valid_next = (it + 1 < ntiles && slot + BM < hi) && resolve_row(p, btr, idx1) >= 0;
+      valid_next = (it + 1 < ntiles && slot + BM < hi) && resolve_slot<kDual>(p, btr, btr2, slot + BM, idx1) >= 0;
     }
     // ---------------------------------------------------------- epilogue
     bool failed = !alive;
@@ -1006,8 +1012,10 @@ cudaError_t launch_tc(const KParams& p, cudaStream_t stream) {
   const int64_t grid = (int64_t)p.T * (p.H / tc_path::HG) * p.num_splits;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  // early row loads and L2 prefetch for a cache that does not stay in L2
-  auto kern = p.big_cache ? tc_path::tc_kernel<true> : tc_path::tc_kernel<false>;
+  // early row loads and L2 prefetch for a cache that does not stay in L2;
+  // the dual-cache form has its own instantiations
+  auto kern = p.dual ? (p.big_cache ? tc_path::tc_kernel<true, true> : tc_path::tc_kernel<false, true>)
+                     : (p.big_cache ? tc_path::tc_kernel<true, false> : tc_path::tc_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_path::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)grid, tc_path::NT, tc_path::SMEM_BYTES, stream>>>(p);

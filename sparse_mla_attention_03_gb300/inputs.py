@@ -45,6 +45,16 @@ class Workload:
     tokens_per_req: int = 1
     decode: bool = False
     meta: dict = dataclasses.field(default_factory=dict)
+    # dual-cache form: a second index list into a second cache (same row format)
+    extra_kv: Optional[torch.Tensor] = None  # uint8 [num_pages2, 64, 656]
+    extra_indices: Optional[torch.Tensor] = None  # int32 [T, ld2]
+    extra_topk: int = 0
+    extra_topk_length: Optional[torch.Tensor] = None  # int32 [T]
+    extra_block_table: Optional[torch.Tensor] = None  # int32 [B, max_pages2]
+
+    @property
+    def dual(self):
+        return self.extra_kv is not None
 
     @property
     def T(self):
@@ -179,6 +189,53 @@ def make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=0, sink=
                   topk=topk, seed=seed, sink=sink))
 
 
+def _ragged_lengths(rng, T, topk, idx):
+    """topk_length ~ U{0..topk} with the entries past it set to -1 (in place)."""
+    lens = rng.integers(0, topk + 1, size=T)
+    cols = np.arange(topk)[None, :]
+    idx[:, :topk] = np.where(cols < lens[:, None], idx[:, :topk], -1)
+    return torch.from_numpy(lens.astype(np.int32))
+
+
+def make_dual_prefill(name, T, H, ctx, topk, extra_ctx, extra_topk, seed=0, sink="normal",
+                      ragged=False) -> Workload:
+    """Dual-cache prefill: a flat first list of ``topk`` unique ids into a cache
+    of ``ctx`` rows and a flat second list of ``extra_topk`` unique ids into a
+    second cache of ``extra_ctx`` rows.  ``ragged``: both lists get
+    topk_length ~ U{0..width} (so either can be empty for a token)."""
+    wl = make_prefill(name, T, H, ctx, topk, seed=seed, sink=sink)
+    rng = np.random.default_rng(seed + 7919)
+    assert extra_ctx % PAGE == 0
+    wl.extra_kv = make_cache(rng, extra_ctx // PAGE)
+    idx2 = unique_rows(rng, T, extra_topk, extra_ctx)
+    if ragged:
+        idx1 = wl.indices.numpy().astype(np.int64)
+        wl.topk_length = _ragged_lengths(rng, T, topk, idx1)
+        wl.indices = torch.from_numpy(idx1.astype(np.int32))
+        wl.extra_topk_length = _ragged_lengths(rng, T, extra_topk, idx2)
+    wl.extra_indices = torch.from_numpy(idx2.astype(np.int32))
+    wl.extra_topk = extra_topk
+    wl.meta.update(extra_ctx=extra_ctx, extra_topk=extra_topk, ragged=ragged)
+    return wl
+
+
+def make_dual_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, extra_ctx_per_req, extra_topk,
+                     seed=0, sink="normal") -> Workload:
+    """Dual-cache decode: the paged decode of ``make_decode`` plus, per
+    request, a second paged cache of ``extra_ctx_per_req`` logical positions
+    (its own shuffled block table) and ``extra_topk`` unique logical ids."""
+    wl = make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=seed, sink=sink)
+    rng = np.random.default_rng(seed + 7919)
+    assert extra_ctx_per_req % PAGE == 0
+    pages2 = extra_ctx_per_req // PAGE
+    wl.extra_kv = make_cache(rng, n_req * pages2)
+    wl.extra_block_table = torch.from_numpy(rng.permutation(n_req * pages2).reshape(n_req, pages2).astype(np.int32))
+    wl.extra_indices = torch.from_numpy(unique_rows(rng, wl.T, extra_topk, extra_ctx_per_req).astype(np.int32))
+    wl.extra_topk = extra_topk
+    wl.meta.update(extra_ctx_per_req=extra_ctx_per_req, extra_topk=extra_topk)
+    return wl
+
+
 # The five workloads, named by what they are.
 def tiny_prefill(seed=0):
     return make_prefill("tiny_prefill_T4_H8_ctx256_k64", T=4, H=8, ctx=256, topk=64,
@@ -205,6 +262,15 @@ def large_prefill(seed=0, T=4096):
                         ctx=131072, topk=2048, seed=seed, neg_prob=0.1)
 
 
+def dual_decode(seed=0, n_req=64):
+    """The dual-cache decode shape "topk 1024 + 2176": 64 requests x 2 tokens,
+    H=64, a 32768-position main cache and an 8192-position second cache per
+    request, both paged."""
+    return make_dual_decode(f"dual_decode_{n_req}req_x2_H64_ctx32768_k1024+ctx8192_k2176_paged", n_req=n_req,
+                            tokens_per_req=2, H=64, ctx_per_req=32768, topk=1024, extra_ctx_per_req=8192,
+                            extra_topk=2176, seed=seed)
+
+
 WORKLOADS = {
     "tiny": tiny_prefill,
     "prefill16k_k512": lambda seed=0: prefill_16k(512, seed),
@@ -212,4 +278,5 @@ WORKLOADS = {
     "fewhead": fewhead_prefill,
     "decode": batched_decode,
     "large": large_prefill,
+    "dual_decode": dual_decode,
 }

@@ -12,10 +12,24 @@ LSE_ABS = 1e-3
 
 def to_dev(wl, device="cuda"):
     d = {}
-    for k in ("q", "kv", "indices", "topk_length", "attn_sink", "block_table"):
+    for k in ("q", "kv", "indices", "topk_length", "attn_sink", "block_table", "extra_kv", "extra_indices",
+              "extra_topk_length", "extra_block_table"):
         v = getattr(wl, k)
         d[k] = None if v is None else v.to(device)
     return d
+
+
+def oracle_dual_for(wl, tokens=None):
+    """The dual-cache oracle on all tokens, or on ``tokens`` only."""
+    sel = None if tokens is None else np.asarray(tokens)
+    q = wl.q.to(torch.float64).numpy() if sel is None else wl.q[torch.as_tensor(sel)].to(torch.float64).numpy()
+    np_ = lambda x: None if x is None else x.numpy()
+    return O.sparse_mla_forward_dual(
+        q, wl.kv.numpy(), wl.indices.numpy(), wl.topk, wl.extra_kv.numpy(), wl.extra_indices.numpy(),
+        wl.extra_topk, wl.sm_scale, topk_length=np_(wl.topk_length), extra_topk_length=np_(wl.extra_topk_length),
+        attn_sink=None if wl.attn_sink is None else wl.attn_sink.numpy().astype(np.float64),
+        block_table=np_(wl.block_table), extra_block_table=np_(wl.extra_block_table),
+        tokens_per_req=wl.tokens_per_req, tokens=sel, q_selected=sel is not None)
 
 
 def oracle_for(wl, tokens=None, indices=None, topk=None, topk_length="wl", attn_sink="wl"):

@@ -90,4 +90,4 @@ def test_explicit_split_arithmetic(lib):
     assert lib.sparse_mla_decode_num_splits(4, 8, 640, 3) == 3
     ws = lib.sparse_mla_decode_workspace_size(128, 64, 2048, 8)
     assert ws == 128 * 64 * 8 * 512 * 4 + 128 * 64 * 8 * 4
-    assert lib.sparse_mla_abi_version() == 1
+    assert lib.sparse_mla_abi_version() == 2

@@ -10,7 +10,7 @@ import torch
 
 import oracle.sparse_mla_oracle as O
 from sparse_mla_attention_03_gb300 import binding, inputs
-from tests.helpers import assert_close, oracle_for, sample_tokens, to_dev
+from tests.helpers import assert_close, oracle_dual_for, oracle_for, sample_tokens, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -191,6 +191,89 @@ def test_cache_beyond_l2_paged_decode(S):
     assert binding.get_error_word() == 0
 
 
+# ----------------------------------------------------------------------------- dual-cache form
+def run_dual(wl, decode=False, num_splits=0):
+    d = to_dev(wl)
+    kw = dict(topk=wl.topk, topk_length=d["topk_length"], extra_topk=wl.extra_topk,
+              extra_topk_length=d["extra_topk_length"], attn_sink=d["attn_sink"], block_table=d["block_table"],
+              extra_block_table=d["extra_block_table"], tokens_per_req=wl.tokens_per_req)
+    if decode:
+        return binding.sparse_mla_decode_dual(d["q"], d["kv"], d["indices"], d["extra_kv"], d["extra_indices"],
+                                              wl.sm_scale, num_splits=num_splits, **kw)
+    return binding.sparse_mla_prefill_dual(d["q"], d["kv"], d["indices"], d["extra_kv"], d["extra_indices"],
+                                           wl.sm_scale, **kw)
+
+
+# topk 200 pads the first list to 256 combined slots, so 128-row tiles of the
+# tcgen05 kernel and 64-row tiles of the warp-MMA kernel both meet padding,
+# the list boundary and a ragged tail
+@pytest.mark.parametrize("H", [8, 16, 64, 128])
+def test_dual_prefill_ragged(H):
+    wl = inputs.make_dual_prefill("dualp", T=7, H=H, ctx=2048, topk=200, extra_ctx=1024, extra_topk=150,
+                                  seed=101 + H, ragged=True)
+    wl.topk_length[0], wl.extra_topk_length[0] = 0, 150   # second list only
+    wl.topk_length[1], wl.extra_topk_length[1] = 200, 0   # first list only
+    wl.topk_length[2], wl.extra_topk_length[2] = 0, 0     # nothing: out 0, lse -inf
+    out, lse = run_dual(wl)
+    assert_close(out, lse, *oracle_dual_for(wl), tag=f"dual_prefill_H{H}")
+    assert binding.get_error_word() == 0
+
+
+@pytest.mark.parametrize("H,S", [(64, 0), (64, 1), (64, 3), (64, 8), (8, 0), (8, 5)])
+def test_dual_decode_paged(H, S):
+    wl = inputs.make_dual_decode("duald", n_req=3, tokens_per_req=2, H=H, ctx_per_req=4096, topk=300,
+                                 extra_ctx_per_req=2048, extra_topk=217, seed=131 + S)
+    out, lse = run_dual(wl, decode=True, num_splits=S)
+    assert_close(out, lse, *oracle_dual_for(wl), tag=f"dual_decode_H{H}_S{S}")
+    assert binding.get_error_word() == 0
+
+
+def test_dual_cache_beyond_l2():
+    # 43 MB + 10.7 MB of caches: the early-load / L2-prefetch variant
+    wl = inputs.make_dual_prefill("dualbig", T=4, H=64, ctx=65536, topk=384, extra_ctx=16384, extra_topk=320,
+                                  seed=151, ragged=True)
+    out, lse = run_dual(wl)
+    assert_close(out, lse, *oracle_dual_for(wl), tag="dual_bigcache")
+    assert binding.get_error_word() == 0
+
+
+def test_dual_index_resolution_bit_exact():
+    wl = inputs.make_dual_decode("dualres", n_req=3, tokens_per_req=2, H=8, ctx_per_req=1024, topk=100,
+                                 extra_ctx_per_req=512, extra_topk=70, seed=161)
+    wl.topk_length = torch.tensor([100, 37, 0, 64, 99, 1], dtype=torch.int32)
+    wl.extra_topk_length = torch.tensor([70, 0, 12, 70, 69, 33], dtype=torch.int32)
+    i2 = wl.extra_indices.clone()
+    i2[0, :3] = torch.tensor([512, -7, 0x7FFFFFFF], dtype=torch.int32)  # out of the 8-page table row
+    wl.extra_indices = i2
+    d = to_dev(wl)
+    rows = binding.sparse_mla_resolve_rows_dual(
+        d["q"], d["kv"], d["indices"], d["extra_kv"], d["extra_indices"], topk=wl.topk,
+        topk_length=d["topk_length"], extra_topk=wl.extra_topk, extra_topk_length=d["extra_topk_length"],
+        block_table=d["block_table"], extra_block_table=d["extra_block_table"], tokens_per_req=2).cpu().numpy()
+    r1 = O.resolve_rows(wl.indices.numpy(), 100, wl.num_pages, wl.topk_length.numpy(),
+                        wl.block_table.numpy(), 2)
+    r2 = O.resolve_rows(wl.extra_indices.numpy(), 70, wl.extra_kv.shape[0], wl.extra_topk_length.numpy(),
+                        wl.extra_block_table.numpy(), 2)
+    base = binding.dual_width(100, 70) - 70
+    assert base == 128 and rows.shape == (6, 198)
+    want = np.full((6, 198), -1, dtype=np.int64)
+    want[:, :100] = r1
+    want[:, base:] = np.where(r2 >= 0, r2 + wl.num_pages * 64, -1)
+    np.testing.assert_array_equal(rows, want)
+    assert binding.get_error_word() & binding.ERRF_INDEX_RANGE
+
+
+def test_dual_rejects_bad_extra():
+    wl = inputs.make_dual_prefill("dualbad", T=2, H=8, ctx=256, topk=64, extra_ctx=128, extra_topk=32, seed=171)
+    d = to_dev(wl)
+    with pytest.raises(ValueError):
+        binding.sparse_mla_prefill_dual(d["q"], d["kv"], d["indices"], d["extra_kv"][:, :32], d["extra_indices"],
+                                        wl.sm_scale)
+    with pytest.raises(binding.SparseMLAError):
+        binding.sparse_mla_prefill_dual(d["q"], d["kv"], d["indices"], d["extra_kv"], d["extra_indices"],
+                                        wl.sm_scale, extra_topk=0)
+
+
 # ----------------------------------------------------------------------------- full-size workloads
 FULL = {
     "prefill16k_k512": (lambda: inputs.prefill_16k(512), "prefill", 48),
@@ -198,6 +281,7 @@ FULL = {
     "fewhead": (inputs.fewhead_prefill, "prefill", 96),
     "decode": (inputs.batched_decode, "decode", 48),
     "large": (inputs.large_prefill, "prefill", 24),
+    "dual_decode": (inputs.dual_decode, "dual_decode", 32),
 }
 
 
@@ -205,9 +289,12 @@ FULL = {
 def test_full_size_workload_sampled(name):
     make, kind, n = FULL[name]
     wl = make()
-    out, lse = (run_prefill(wl) if kind == "prefill" else run_decode(wl))
+    if kind == "dual_decode":
+        out, lse = run_dual(wl, decode=True)
+    else:
+        out, lse = (run_prefill(wl) if kind == "prefill" else run_decode(wl))
     toks = sample_tokens(wl.T, n, seed=5, must=(0, wl.T - 1))
-    ref = oracle_for(wl, tokens=toks)
+    ref = oracle_dual_for(wl, tokens=toks) if wl.dual else oracle_for(wl, tokens=toks)
     tt = torch.as_tensor(toks, device=out.device)
     assert_close(out[tt], lse[tt], *ref, tag=name)
     assert torch.isfinite(out).all()

@@ -378,3 +378,104 @@ def test_planted_mistakes_are_caught(monkeypatch):
             check_dense_vs_sdpa(O.sparse_mla_forward, with_sink=with_sink)
             check_golden()
         monkeypatch.setattr(O, "attend_one", orig_attend)
+
+
+# ----------------------------------------------------------------------------- dual-cache form
+def _dual_case(seed=21):
+    return inputs.make_dual_prefill("dualpin", T=5, H=3, ctx=256, topk=70, extra_ctx=192, extra_topk=45,
+                                    seed=seed, ragged=True)
+
+
+def _call_dual(fwd, wl, kv=None, extra_kv=None, **kw):
+    args = dict(topk_length=None if wl.topk_length is None else wl.topk_length.numpy(),
+                extra_topk_length=None if wl.extra_topk_length is None else wl.extra_topk_length.numpy(),
+                attn_sink=wl.attn_sink.numpy(), extra_block_table=None if wl.extra_block_table is None
+                else wl.extra_block_table.numpy(), block_table=None if wl.block_table is None
+                else wl.block_table.numpy(), tokens_per_req=wl.tokens_per_req)
+    args.update(kw)
+    return fwd(q_f64(wl), wl.kv.numpy() if kv is None else kv, wl.indices.numpy(), wl.topk,
+               wl.extra_kv.numpy() if extra_kv is None else extra_kv, wl.extra_indices.numpy(), wl.extra_topk,
+               wl.sm_scale, **args)
+
+
+def check_dual(fwd=None):
+    """The dual-cache form against the one-list form and a library routine."""
+    fwd = fwd or O.sparse_mla_forward_dual
+    wl = _dual_case()
+    out, lse = _call_dual(fwd, wl)
+    l1, l2 = wl.topk_length.numpy(), wl.extra_topk_length.numpy()
+    # (a) both caches stacked into one cache, the second list's ids shifted past
+    # the first cache's rows, the lengths written as -1 padding
+    kv1 = wl.kv.numpy().reshape(-1, 656)
+    kv2 = wl.extra_kv.numpy().reshape(-1, 656)
+    stack = np.concatenate([kv1, kv2])
+    i1 = wl.indices.numpy().astype(np.int64)
+    i1 = np.where(np.arange(wl.topk)[None, :] < l1[:, None], i1, -1)
+    i2 = wl.extra_indices.numpy().astype(np.int64)
+    i2 = np.where(np.arange(wl.extra_topk)[None, :] < l2[:, None], i2 + kv1.shape[0], -1)
+    one = np.concatenate([i1, i2], axis=1).astype(np.int32)
+    out_s, lse_s = O.sparse_mla_forward(q_f64(wl), stack, one, one.shape[1], wl.sm_scale,
+                                        attn_sink=wl.attn_sink.numpy())
+    np.testing.assert_allclose(out, out_s, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_s, rtol=1e-12, atol=1e-12)
+    # (b) an empty second list is the one-list form over the first list
+    out_e, lse_e = _call_dual(fwd, wl, extra_topk_length=np.zeros(wl.T, dtype=np.int32))
+    out_1, lse_1 = O.sparse_mla_forward(q_f64(wl), wl.kv.numpy(), wl.indices.numpy(), wl.topk, wl.sm_scale,
+                                        topk_length=l1, attn_sink=wl.attn_sink.numpy())
+    np.testing.assert_allclose(out_e, out_1, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse_e, lse_1, rtol=1e-12, atol=1e-12)
+    # (c) swapping the two lists (with their caches) changes nothing
+    out_w, lse_w = fwd(q_f64(wl), wl.extra_kv.numpy(), wl.extra_indices.numpy(), wl.extra_topk, wl.kv.numpy(),
+                       wl.indices.numpy(), wl.topk, wl.sm_scale, topk_length=l2, extra_topk_length=l1,
+                       attn_sink=wl.attn_sink.numpy())
+    np.testing.assert_allclose(out_w, out, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(lse_w, lse, rtol=1e-12, atol=1e-12)
+    # (d) one cache, its rows split between the two lists: dense attention
+    # over the whole context through torch SDPA, with the sink as an extra key
+    dense = tiny_dense_workload(seed=5, H=3, ctx=128)
+    sink = np.array([0.3, -1.2, 2.0])
+    kvd = dense.kv.numpy()
+    perm = dense.indices.numpy()
+    od, ld = fwd(q_f64(dense), kvd, perm[:, :50], 50, kvd, perm[:, 50:], 78, dense.sm_scale, attn_sink=sink)
+    K = dequant_via_torch(kvd.reshape(-1, 656)).numpy()
+    for t in range(dense.T):
+        ref_o, ref_l = sdpa_dense(q_f64(dense)[t], K, dense.sm_scale, sink)
+        np.testing.assert_allclose(od[t], ref_o, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(ld[t], ref_l, rtol=1e-12, atol=1e-12)
+    # (e) a paged second list equals the flat list of its physical rows
+    wd = inputs.make_dual_decode("dualpaged", n_req=2, tokens_per_req=2, H=2, ctx_per_req=256, topk=40,
+                                 extra_ctx_per_req=128, extra_topk=30, seed=8)
+    op, lp = _call_dual(fwd, wd)
+    bt2 = wd.extra_block_table.numpy().astype(np.int64)
+    li = wd.extra_indices.numpy().astype(np.int64)
+    req = (np.arange(wd.T) // wd.tokens_per_req)[:, None]
+    phys = (bt2[req, li // 64] * 64 + li % 64).astype(np.int32)
+    of, lf = fwd(q_f64(wd), wd.kv.numpy(), wd.indices.numpy(), wd.topk, wd.extra_kv.numpy(), phys, wd.extra_topk,
+                 wd.sm_scale, attn_sink=wd.attn_sink.numpy(), block_table=wd.block_table.numpy(),
+                 tokens_per_req=wd.tokens_per_req)
+    np.testing.assert_array_equal(op, of)
+    np.testing.assert_array_equal(lp, lf)
+
+
+def test_dual_cache_form_against_one_list_and_sdpa():
+    check_dual()
+
+
+def test_dual_cache_planted_mistakes_are_caught():
+    def second_list_in_first_cache(q, kv, i1, k1, kv2, i2, k2, sm_scale, **kw):
+        return O.sparse_mla_forward_dual(q, kv, i1, k1, kv, i2, k2, sm_scale, **kw)
+
+    def two_softmaxes_averaged(q, kv, i1, k1, kv2, i2, k2, sm_scale, topk_length=None, extra_topk_length=None,
+                               attn_sink=None, block_table=None, extra_block_table=None, tokens_per_req=1):
+        a = O.sparse_mla_forward(q, kv, i1, k1, sm_scale, topk_length=topk_length, attn_sink=attn_sink,
+                                 block_table=block_table, tokens_per_req=tokens_per_req)
+        b = O.sparse_mla_forward(q, kv2, i2, k2, sm_scale, topk_length=extra_topk_length, attn_sink=attn_sink,
+                                 block_table=extra_block_table, tokens_per_req=tokens_per_req)
+        return 0.5 * (a[0] + b[0]), np.logaddexp(a[1], b[1])
+
+    def second_length_ignored(q, kv, i1, k1, kv2, i2, k2, sm_scale, extra_topk_length=None, **kw):
+        return O.sparse_mla_forward_dual(q, kv, i1, k1, kv2, i2, k2, sm_scale, **kw)
+
+    for bad in (second_list_in_first_cache, two_softmaxes_averaged, second_length_ignored):
+        with pytest.raises(AssertionError):
+            check_dual(bad)
