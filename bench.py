@@ -91,6 +91,27 @@ def work_of(wl):
     return dict(valid=v, flops=flops, bytes=gather + io, gather_bytes=gather)
 
 
+def dram_traffic(workload):
+    """DRAM bytes per launch of the attention kernel from a committed ncu capture
+    (profiles/dram_traffic.json), or None when there is none for this workload or
+    the kernel sources changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        rec = json.load(f).get(workload)
+    if not rec:
+        return None, None
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec["sources_sha256"]:
+        return None, "kernel changed since the capture"
+    return rec["dram_bytes_per_launch"], rec["capture"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -117,8 +138,9 @@ def _oracle_chunk(args):
     return len(toks)
 
 
-def oracle_time(wl, n_tokens, cores):
-    """Oracle wall time on n_tokens tokens spread over `cores` spawn processes."""
+def oracle_time(wl, n_tokens, cores, pool=None):
+    """Oracle wall time on n_tokens tokens spread over `cores` spawn processes
+    (a pool of them is made here unless one is passed in)."""
     import numpy as np
     import torch
     toks = np.arange(min(n_tokens, wl.T))
@@ -133,12 +155,18 @@ def oracle_time(wl, n_tokens, cores):
              np_(wl.extra_block_table)) if wl.dual else None
     jobs = [(wl.q[torch.as_tensor(c)].to(torch.float64).numpy(), kv, idx, wl.topk, wl.sm_scale, tl, sink, bt,
              wl.tokens_per_req, c, extra) for c in chunks]
-    ctx = mp.get_context("spawn")
-    with ctx.Pool(len(jobs), initializer=_pin_threads) as pool:
+    own = pool is None
+    if own:
+        pool = mp.get_context("spawn").Pool(cores, initializer=_pin_threads)
+    try:
         pool.map(_oracle_chunk, jobs[:1])  # warm the workers' imports
         t0 = time.perf_counter()
         n = sum(pool.map(_oracle_chunk, jobs))
         dt = time.perf_counter() - t0
+    finally:
+        if own:
+            pool.close()
+            pool.join()
     return n, dt
 
 
@@ -277,10 +305,14 @@ def run_ours(args, rank, world, local_rank):
             ws = torch.empty(max(256, binding.decode_workspace_size(wl.T, wl.H, width, args.num_splits)),
                              dtype=torch.uint8, device=dev)
         call = make_call(spec["kind"], binding, d, wl, out, lse, ws, args.num_splits)
-        parts.append(dict(tag=tag, wl=wl, d=d, out=out, lse=lse, ws=ws, call=call, work=work_of(wl)))
+        # kernels per call: the attention kernel, plus the combine when decode splits
+        launches = 1
+        if spec["kind"] != "prefill":
+            launches = 1 if binding.decode_num_splits(wl.T, wl.H, width, args.num_splits) == 1 else 2
+        parts.append(dict(tag=tag, wl=wl, d=d, out=out, lse=lse, ws=ws, call=call, work=work_of(wl),
+                          launches=launches))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_part = 1 if spec["kind"] == "prefill" else 2
 
     def barrier():
         if world > 1:
@@ -324,6 +356,12 @@ def run_ours(args, rank, world, local_rank):
         roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm"], unit="GB/s",
                     frac=round(achieved / peaks["hbm"], 4), traffic=None,
                     peak_source=f"{peaks['src']} HBM copy bandwidth")
+    traffic, src = dram_traffic(args.workload)
+    if traffic is not None:
+        roof["traffic"] = traffic
+        roof["traffic_unit"] = "bytes per launch (mean), ncu dram__bytes_read.sum + dram__bytes_write.sum"
+    if src is not None:
+        roof["traffic_source"] = src
     roof["per_launch"] = {p["tag"]: dict(ms=round(statistics.mean(per_part_ms[j]), 4),
                                          tflops=round(p["work"]["flops"] / (statistics.mean(per_part_ms[j]) / 1e3) / 1e12, 2),
                                          gbs=round(p["work"]["bytes"] / (statistics.mean(per_part_ms[j]) / 1e3) / 1e9, 1))
@@ -343,7 +381,7 @@ def run_ours(args, rank, world, local_rank):
                    "num_splits": args.num_splits if spec["kind"] != "prefill" else None},
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": args.steps * len(parts) * launches_per_part,
+        "gpu_launches": args.steps * sum(p["launches"] for p in parts),
         "clocks": clk.summary(),
         "wall_s": round(wall, 3),
     }
@@ -384,17 +422,24 @@ def run_e2e(args, parts, dev, stream, world):
             "d2h_bytes_per_step": d2h, "steps": steps}
 
 
-def cpu_baseline(parts_or_wls, budget_tokens):
+def cpu_baseline(parts_or_wls, budget_tokens, min_seconds=10.0, max_passes=12):
+    """The oracle timed on the first budget_tokens tokens of each part, repeated
+    until about min_seconds of CPU work have been measured (bounded passes)."""
     cores = min(host_cores(), 32)
-    n_tot, t_tot = 0, 0.0
+    n_tot, t_tot, passes = 0, 0.0, 0
     descs = []
-    for wl in parts_or_wls:
-        n, dt = oracle_time(wl, budget_tokens, cores)
-        n_tot += n
-        t_tot += dt
-        descs.append(f"{wl.name}: first {n} tokens")
+    with mp.get_context("spawn").Pool(cores, initializer=_pin_threads) as pool:
+        while passes < max_passes and (passes == 0 or t_tot < min_seconds):
+            for wl in parts_or_wls:
+                n, dt = oracle_time(wl, budget_tokens, cores, pool)
+                n_tot += n
+                t_tot += dt
+                if passes == 0:
+                    descs.append(f"{wl.name}: first {n} tokens")
+            passes += 1
     return {"value": round(n_tot / t_tot, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "; ".join(descs) + f" (fp64 numpy oracle, {cores} spawn processes, {t_tot:.1f} s)"}
+            "sample": "; ".join(descs) + f", {passes} passes (fp64 numpy oracle, {cores} spawn processes, "
+                      f"{t_tot:.1f} s)"}
 
 
 def run_reference(args):

@@ -147,7 +147,9 @@ int sparse_mla_prefill(const smla_args* args, smla_stream_t stream);
  * and its LSE) to the caller's workspace; a combine kernel then merges the
  * partials with weights exp(lse_s - lse) and applies the sink (FlashInfer PR
  * #4802, "Runner and CUDA graphs": split-K scratch owned by the caller; AppMana
- * releases, "decode H6: warp-wide combine").
+ * releases, "decode H6: warp-wide combine").  With one split (automatic for
+ * few tokens x long lists) the attention kernel writes out and lse directly
+ * and no combine runs; the workspace is then not touched.
  *
  *  num_splits   0 = automatic, else 1..64 (reduced so that no split is empty
  *               of slots: effective splits = ceil(topk / chunk)).

@@ -244,10 +244,17 @@ int decode_launch(smla::KParams p, int width, int num_splits, void* workspace, s
   const int chunks = (width + 63) / 64;
   p.num_splits = S;
   p.split_len = ((chunks + S - 1) / S) * 64;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (S == 1) {
+    // one split: the attention kernel writes out and lse itself (the prefill
+    // epilogue), with no partials and no combine
+    cudaError_t e = smla::launch_attention(p, st);
+    if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    return SMLA_OK;
+  }
   const size_t o_bytes = (size_t)p.T * p.H * S * SMLA_D_V * sizeof(float);
   p.ws_o = static_cast<float*>(workspace);
   p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = smla::launch_attention(p, st);
   if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode split launch: %s", cudaGetErrorString(e));
   e = smla::launch_combine(p, st);

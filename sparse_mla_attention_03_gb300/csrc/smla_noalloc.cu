@@ -84,13 +84,18 @@ extern "C" int sparse_mla_decode_noalloc(const smla_args* a, int32_t num_splits,
   const int chunks = (a->topk + 63) / 64;
   p.num_splits = S;
   p.split_len = ((chunks + S - 1) / S) * 64;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (S == 1) {  // one split: final outputs straight from the attention kernel
+    cudaError_t e = smla::launch_attention(p, st);
+    if (e != cudaSuccess) return smla::host::set_error(SMLA_ERR_CUDA, cudaGetErrorString(e));
+    return SMLA_OK;
+  }
   // Every partial slot [t, h, s] is written by the split kernel before the
   // combine reads it (empty splits write lse = -inf), so nothing left in the
   // array by an earlier call needs clearing.
   const size_t o_bytes = (size_t)a->T * a->H * S * SMLA_D_V * sizeof(float);
   p.ws_o = static_cast<float*>(scratch);
   p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) + ((o_bytes + 255) / 256) * 256);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = smla::launch_attention(p, st);
   if (e != cudaSuccess) return smla::host::set_error(SMLA_ERR_CUDA, cudaGetErrorString(e));
   e = smla::launch_combine(p, st);
