@@ -56,6 +56,12 @@ struct Layout {
   static constexpr int total = qmul + HG * 4;
 };
 
+// 16 zero bytes to shared memory (the slot of an invalid row; no global
+// address is formed for it, so an empty cache may have a null pointer).
+__device__ __forceinline__ void sts_zero16(uint32_t dst) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(dst), "r"(0) : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
@@ -140,8 +146,10 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
       const int rr = __shfl_sync(0xffffffffu, row, r & 15);
       if (f < 16 * 41) {
         const uint32_t dst = smem_u32(base + r * TS + swz(warp * 16 + r, ch) * 16);
-        const uint8_t* src = rr >= 0 ? row_ptr<kDual>(p, rr) + ch * 16 : p.kv;
-        cp_async16(dst, src, rr >= 0 ? 16 : 0);
+        if (rr >= 0)
+          cp_async16(dst, row_ptr<kDual>(p, rr) + ch * 16, 16);
+        else
+          sts_zero16(dst);
       }
     }
     return __ballot_sync(0xffffffffu, lane < 16 && row >= 0) & 0xFFFFu;

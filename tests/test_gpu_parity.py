@@ -263,6 +263,21 @@ def test_dual_index_resolution_bit_exact():
     assert binding.get_error_word() & binding.ERRF_INDEX_RANGE
 
 
+@pytest.mark.parametrize("H", [8, 64])
+def test_empty_first_cache(H):
+    # a cache with no pages (a null pointer): every index of the first list is
+    # padding or out of range, so only the second list contributes
+    wl = inputs.make_dual_prefill("dualempty", T=4, H=H, ctx=256, topk=96, extra_ctx=1024, extra_topk=200,
+                                  seed=181)
+    wl.kv = torch.empty((0, 64, 656), dtype=torch.uint8)
+    idx = wl.indices.clone()
+    idx[:, ::2] = -1
+    wl.indices = idx
+    out, lse = run_dual(wl)
+    assert_close(out, lse, *oracle_dual_for(wl), tag=f"dual_empty_first_H{H}")
+    assert binding.get_error_word() & binding.ERRF_INDEX_RANGE  # the other indices are out of range
+
+
 def test_dual_rejects_bad_extra():
     wl = inputs.make_dual_prefill("dualbad", T=2, H=8, ctx=256, topk=64, extra_ctx=128, extra_topk=32, seed=171)
     d = to_dev(wl)
