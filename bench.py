@@ -56,6 +56,8 @@ def workloads(tokens=None):
                      parts=[("all", lambda s: inputs.tiny_prefill(seed=s))]),
         "dual_decode": dict(name="dual_decode_64req_x2_H64_ctx32768_k1024+ctx8192_k2176_paged", kind="dual_decode",
                             bound="hbm", parts=[("all", lambda s: inputs.dual_decode(seed=s))]),
+        "prefill16k_int8": dict(name=f"prefill_T{T16}_H64_ctx16384_k1024_int8", kind="prefill", bound="tensor",
+                                parts=[("k1024", lambda s: inputs.prefill_16k_int8(1024, seed=s, T=T16))]),
     }
 
 
@@ -126,15 +128,15 @@ def load_peaks():
 def _oracle_chunk(args):
     import numpy as np
     import oracle.sparse_mla_oracle as O
-    (q, kv, idx, topk, sm, tl, sink, bt, tpr, toks, extra) = args
+    (q, kv, idx, topk, sm, tl, sink, bt, tpr, toks, extra, fmt) = args
     if extra is None:
         O.sparse_mla_forward(q, kv, idx, topk, sm, topk_length=tl, attn_sink=sink, block_table=bt,
-                             tokens_per_req=tpr, tokens=toks, q_selected=True)
+                             tokens_per_req=tpr, tokens=toks, q_selected=True, kv_format=fmt)
     else:
         kv2, idx2, topk2, tl2, bt2 = extra
         O.sparse_mla_forward_dual(q, kv, idx, topk, kv2, idx2, topk2, sm, topk_length=tl, extra_topk_length=tl2,
                                   attn_sink=sink, block_table=bt, extra_block_table=bt2, tokens_per_req=tpr,
-                                  tokens=toks, q_selected=True)
+                                  tokens=toks, q_selected=True, kv_format=fmt)
     return len(toks)
 
 
@@ -154,7 +156,7 @@ def oracle_time(wl, n_tokens, cores, pool=None):
     extra = (wl.extra_kv.numpy(), wl.extra_indices.numpy(), wl.extra_topk, np_(wl.extra_topk_length),
              np_(wl.extra_block_table)) if wl.dual else None
     jobs = [(wl.q[torch.as_tensor(c)].to(torch.float64).numpy(), kv, idx, wl.topk, wl.sm_scale, tl, sink, bt,
-             wl.tokens_per_req, c, extra) for c in chunks]
+             wl.tokens_per_req, c, extra, wl.kv_format) for c in chunks]
     own = pool is None
     if own:
         pool = mp.get_context("spawn").Pool(cores, initializer=_pin_threads)
@@ -263,13 +265,14 @@ def make_call(kind, binding, d, wl, out, lse, ws, num_splits):
             binding.sparse_mla_prefill(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
                                        topk_length=d["topk_length"], attn_sink=d["attn_sink"],
                                        block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
-                                       out=out, lse=lse, stream=stream)
+                                       out=out, lse=lse, stream=stream, kv_format=wl.kv_format)
     elif kind == "decode":
         def call(stream=None):
             binding.sparse_mla_decode(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
                                       topk_length=d["topk_length"], attn_sink=d["attn_sink"],
                                       block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
-                                      num_splits=num_splits, workspace=ws, out=out, lse=lse, stream=stream)
+                                      num_splits=num_splits, workspace=ws, out=out, lse=lse, stream=stream,
+                                      kv_format=wl.kv_format)
     else:
         def call(stream=None):
             binding.sparse_mla_decode_dual(d["q"], d["kv"], d["indices"], d["extra_kv"], d["extra_indices"],
@@ -278,7 +281,7 @@ def make_call(kind, binding, d, wl, out, lse, ws, num_splits):
                                            attn_sink=d["attn_sink"], block_table=d["block_table"],
                                            extra_block_table=d["extra_block_table"],
                                            tokens_per_req=wl.tokens_per_req, num_splits=num_splits, workspace=ws,
-                                           out=out, lse=lse, stream=stream)
+                                           out=out, lse=lse, stream=stream, kv_format=wl.kv_format)
     return call
 
 
@@ -477,7 +480,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["prefill16k", "fewhead", "decode", "large", "tiny", "dual_decode"],
+    ap.add_argument("--workload", choices=["prefill16k", "fewhead", "decode", "large", "tiny", "dual_decode",
+                                           "prefill16k_int8"],
                     default="prefill16k")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--seed", type=int, default=0)

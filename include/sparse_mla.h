@@ -48,7 +48,8 @@
  *     nothing), SMLA_ERR_UNSUPPORTED, SMLA_ERR_CUDA (a launch failed).
  *     sparse_mla_last_error() gives a message for the calling thread.
  *   - Range of the cache values: the kernels hold dequantised values in fp16,
- *     so every |e4m3 * scale| must be at most 65504 (scales at most 128).
+ *     so every |code * scale| must be at most 65504 (scales at most 128,
+ *     in either cache format).
  */
 #ifndef SPARSE_MLA_H_
 #define SPARSE_MLA_H_
@@ -86,6 +87,22 @@ enum {
 #define SMLA_MAX_SPLITS 64
 
 /*
+ * Cache formats (the code bytes [0:512) of a 656-byte row; the per-128 fp32
+ * scales and the bf16 rope are the same in both):
+ *  SMLA_KV_E4M3  OCP FP8 E4M3FN codes, the DSv3.2 layout (FlashInfer PR
+ *                #4802, KV layout note; power-of-two scales).
+ *  SMLA_KV_INT8  signed int8 codes (two's complement), value = code * scale.
+ *                The AppMana releases page names the INT8 latent-cache kernels
+ *                (fwd_sparse_int8_decode_mla, fwd_sparse_int8_prefill_mla;
+ *                "int8 width 1024" at the 16k footprint) but prints no byte
+ *                layout; this keeps the DSv3.2 row layout with int8 codes in
+ *                place of e4m3, the plainest reading.  Scales need not be
+ *                powers of two; the kernels round them to fp16.
+ */
+#define SMLA_KV_E4M3 0
+#define SMLA_KV_INT8 1
+
+/*
  * Arguments shared by prefill and decode.  Strides are in ELEMENTS of the
  * pointed-to type.
  *
@@ -103,6 +120,7 @@ enum {
  *  out          bf16 [T, H, 512]: head stride 512, token stride out_stride_t
  *               (>= H*512, multiple of 4), 8-byte aligned; written in place.
  *  lse          fp32 [T, H]: token stride lse_stride_t (>= H).
+ *  kv_format    SMLA_KV_E4M3 or SMLA_KV_INT8 (see above).
  *  H in [1, 128]; T >= 0; topk >= 1.
  */
 typedef struct smla_args {
@@ -123,7 +141,7 @@ typedef struct smla_args {
   float sm_scale;
   int32_t T;
   int32_t H;
-  int32_t reserved0; /* must be 0 */
+  int32_t kv_format; /* SMLA_KV_E4M3 (0) or SMLA_KV_INT8 (1), for every cache of the call */
   void* out;
   int64_t out_stride_t;
   float* lse;

@@ -52,8 +52,9 @@ one valid index; identical rows; permutation invariance; paged == flat after a
 page shuffle; truncation == -1 padding; the split/merge algebra against the
 one-shot result; the dual-cache form against the one-list form (two caches
 stacked into one with the second list's ids shifted, an empty second list,
-the two lists swapped, and one list split in two over the same cache).  Every
-function below has at least one of these pins.
+the two lists swapped, and one list split in two over the same cache); the
+int8 decoder against torch's int8 view over every byte and SDPA on an int8
+cache.  Every function below has at least one of these pins.
 """
 from __future__ import annotations
 
@@ -91,6 +92,11 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
     return sign * val
 
 
+def int8_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Signed int8 codes (two's complement bytes) to float64."""
+    return np.asarray(codes, dtype=np.uint8).view(np.int8).astype(np.float64)
+
+
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """bf16 is the top half of an IEEE binary32: widen the bits and reinterpret."""
     u = np.asarray(bits).astype(np.uint32) << np.uint32(16)
@@ -106,17 +112,21 @@ def f32_le_bytes_to_f64(b: np.ndarray) -> np.ndarray:
 # ----------------------------------------------------------------------------
 # Row decoding (the dequantisation step)
 # ----------------------------------------------------------------------------
-def decode_rows(rows: np.ndarray) -> np.ndarray:
+def decode_rows(rows: np.ndarray, kv_format: str = "e4m3") -> np.ndarray:
     """Dequantise latent rows: uint8 ``[n, 656]`` -> float64 ``[n, 576]``.
 
-    ``k[i] = e4m3(byte[i]) * scale[i // 128]`` for ``i < 512`` and
+    ``k[i] = code(byte[i]) * scale[i // 128]`` for ``i < 512`` and
     ``k[512 + i] = bf16(rope[i])`` for ``i < 64`` (FlashInfer PR #4802, KV
-    layout note).  V of the same row is ``k[:512]``.
+    layout note).  V of the same row is ``k[:512]``.  ``code`` is e4m3, or
+    for ``kv_format="int8"`` a signed byte: the AppMana releases page names
+    INT8 latent-cache kernels without a byte layout, read here as the same
+    row with int8 codes in place of e4m3.
     """
     rows = np.asarray(rows, dtype=np.uint8)
     assert rows.ndim == 2 and rows.shape[1] == ROW_BYTES, rows.shape
+    assert kv_format in ("e4m3", "int8"), kv_format
     n = rows.shape[0]
-    nope = e4m3_to_f64(rows[:, :D_NOPE])
+    nope = (int8_to_f64 if kv_format == "int8" else e4m3_to_f64)(rows[:, :D_NOPE])
     scales = f32_le_bytes_to_f64(rows[:, _SCALE_OFF:_ROPE_OFF]).reshape(n, D_NOPE // SCALE_BLOCK)
     nope = nope * np.repeat(scales, SCALE_BLOCK, axis=1)
     rope_bits = np.ascontiguousarray(rows[:, _ROPE_OFF:ROW_BYTES]).view("<u2")
@@ -194,7 +204,7 @@ def attend_one(q_t, K, sm_scale, sink=None):
 
 def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
                        attn_sink=None, block_table=None, tokens_per_req=1,
-                       tokens=None, q_selected=False):
+                       tokens=None, q_selected=False, kv_format="e4m3"):
     """Sparse MLA forward for the selected tokens (all tokens by default).
 
     ``q``: float64 ``[T, H, 576]`` (bf16 values widened exactly), or only the
@@ -219,7 +229,7 @@ def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
     sink = None if attn_sink is None else np.asarray(attn_sink, dtype=np.float64)
     for i, t in enumerate(sel):
         r = rows[i]
-        K = decode_rows(kv[r[r >= 0]])
+        K = decode_rows(kv[r[r >= 0]], kv_format)
         out[i], lse[i] = attend_one(q[i] if q_selected else q[t], K, sm_scale, sink)
     return out, lse
 
@@ -227,7 +237,7 @@ def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
 def sparse_mla_forward_dual(q, kv_cache, indices, topk, extra_kv_cache, extra_indices, extra_topk,
                             sm_scale, topk_length=None, extra_topk_length=None, attn_sink=None,
                             block_table=None, extra_block_table=None, tokens_per_req=1,
-                            tokens=None, q_selected=False):
+                            tokens=None, q_selected=False, kv_format="e4m3"):
     """Dual-cache form: one sink softmax per token over the valid slots of two
     index lists, the first resolved in ``kv_cache`` and the second in
     ``extra_kv_cache`` (FlashInfer PR #4802: the DSv4 secondary cache with its
@@ -257,7 +267,8 @@ def sparse_mla_forward_dual(q, kv_cache, indices, topk, extra_kv_cache, extra_in
     sink = None if attn_sink is None else np.asarray(attn_sink, dtype=np.float64)
     for i, t in enumerate(sel):
         r1, r2 = rows1[i], rows2[i]
-        K = np.concatenate([decode_rows(kv1[r1[r1 >= 0]]), decode_rows(kv2[r2[r2 >= 0]])], axis=0)
+        K = np.concatenate([decode_rows(kv1[r1[r1 >= 0]], kv_format), decode_rows(kv2[r2[r2 >= 0]], kv_format)],
+                           axis=0)
         out[i], lse[i] = attend_one(q[i] if q_selected else q[t], K, sm_scale, sink)
     return out, lse
 

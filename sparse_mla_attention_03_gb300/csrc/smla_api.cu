@@ -59,7 +59,8 @@ int validate(const smla_args* a) {
   if (a->T < 0) return fail(SMLA_ERR_INVALID, "T = %d < 0", a->T);
   if (a->H < 1 || a->H > SMLA_MAX_HEADS) return fail(SMLA_ERR_INVALID, "H = %d not in [1, 128]", a->H);
   if (a->topk < 1) return fail(SMLA_ERR_INVALID, "topk = %d < 1", a->topk);
-  if (a->reserved0 != 0) return fail(SMLA_ERR_INVALID, "reserved0 must be 0");
+  if (a->kv_format != SMLA_KV_E4M3 && a->kv_format != SMLA_KV_INT8)
+    return fail(SMLA_ERR_INVALID, "kv_format = %d is neither SMLA_KV_E4M3 nor SMLA_KV_INT8", a->kv_format);
   if (!(a->sm_scale == a->sm_scale) || a->sm_scale > 3.0e38f || a->sm_scale < -3.0e38f)
     return fail(SMLA_ERR_INVALID, "sm_scale is not finite");
   if (a->T == 0) return SMLA_OK;
@@ -125,6 +126,7 @@ smla::KParams make_params(const smla_args* a, int dev) {
   // meet with L2 prefetch and earlier register loads.
   p.big_cache = (int64_t)a->num_pages * SMLA_PAGE * SMLA_ROW_BYTES > g_l2_bytes[dev] / 4 ? 1 : 0;
   p.err = g_err_ptr[dev];
+  p.kv_format = a->kv_format;
   // one list: the second-list fields stay inert
   p.dual = 0;
   p.x_base = 0x7FFFFFFF;
@@ -266,7 +268,7 @@ int decode_launch(smla::KParams p, int width, int num_splits, void* workspace, s
 
 extern "C" {
 
-int32_t sparse_mla_abi_version(void) { return 2; }
+int32_t sparse_mla_abi_version(void) { return 3; }
 
 const char* sparse_mla_last_error(void) { return g_last_error; }
 

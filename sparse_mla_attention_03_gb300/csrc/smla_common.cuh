@@ -74,7 +74,7 @@ struct KParams {
   const int32_t* block_table2;  // nullptr: flat row ids
   int64_t bt2_stride;
   int32_t bt2_cols;
-  int32_t reserved_;
+  int32_t kv_format;  // 0: e4m3 codes, 1: int8 codes (both caches)
   const int32_t* indices2;
   int64_t idx2_stride_t;
   const int32_t* topk_length2;  // nullptr: topk2
@@ -224,6 +224,29 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   lo = e4m3x2_to_f16x2((uint16_t)(w & 0xFFFFu));
   hi = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+}
+
+// Four signed int8 codes (byte 0 first) -> two f16x2, exactly: each code c is
+// biased to c + 128 in [0, 255] and placed as the low mantissa byte of the
+// f16 0x6400 (= 1024, whose unit in the last place is 1), which reads
+// 1152 + c; subtracting 1152 is exact for every integer below 2048.
+__device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  const uint32_t b = 0x64646464u, off = 0x64806480u;  // f16x2 (1152, 1152)
+  uint32_t l, h;
+  asm("prmt.b32 %0, %1, %2, 0x4140;\n" : "=r"(l) : "r"(x), "r"(b));
+  asm("prmt.b32 %0, %1, %2, 0x4342;\n" : "=r"(h) : "r"(x), "r"(b));
+  asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(l), "r"(off));
+  asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"(h), "r"(off));
+}
+
+// Cache codes of either format -> f16 (unscaled).
+template <bool kInt8>
+__device__ __forceinline__ void codes4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if (kInt8)
+    s8x4_to_f16x2x2(w, lo, hi);
+  else
+    e4m3x4_to_f16x2x2(w, lo, hi);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

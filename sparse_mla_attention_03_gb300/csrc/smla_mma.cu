@@ -10,7 +10,7 @@
 //    rows; warp w gathers rows 16w..16w+15 of each tile with 16-byte cp.async
 //    (coalesced: a warp copies whole 656-byte rows), two tiles in flight.
 //  * S^T = K Q^T: warp w computes its 16 rows x all heads of the group.  The
-//    e4m3 codes are converted to f16 in registers (one cvt per two codes, no
+//    e4m3 (or int8) codes are converted to f16 in registers (one cvt per two codes, no
 //    scale); the per-128 scale multiplies the fp32 partial sum of each
 //    128-dim group.  The rope part runs as a bf16 MMA.  The contraction index
 //    is permuted inside each 64-dim block so that a thread's fragment is 16
@@ -69,7 +69,7 @@ __device__ __forceinline__ uint32_t wsel(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
-template <int NH8, int NST, bool kDual>
+template <int NH8, int NST, bool kDual, bool kInt8>
 __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams p) {
   constexpr int HG = NH8 * 8;
   using L = Layout<NH8, NST>;
@@ -221,8 +221,8 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
           for (int ss = 0; ss < 2; ++ss) {
             const int s = 2 * s2 + ss;
             uint32_t a0, a1, a2, a3;
-            e4m3x4_to_f16x2x2(wsel(ka, s), a0, a2);
-            e4m3x4_to_f16x2x2(wsel(kb, s), a1, a3);
+            codes4_to_f16x2x2<kInt8>(wsel(ka, s), a0, a2);
+            codes4_to_f16x2x2<kInt8>(wsel(kb, s), a1, a3);
 #pragma unroll
             for (int n = 0; n < NH8; ++n)
               mma_f16_16816(tmp[n], a0, a1, a2, a3, ss ? qv[n].z : qv[n].x, ss ? qv[n].w : qv[n].y);
@@ -340,10 +340,10 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
         const uint32_t x0 = prmt(t01l, t23l, 0x5410), x1 = prmt(t01l, t23l, 0x7632);
         const uint32_t x2 = prmt(t01h, t23h, 0x5410), x3 = prmt(t01h, t23h, 0x7632);
         uint32_t l0, h0_, l1, h1_, l2, h2_, l3, h3_;
-        e4m3x4_to_f16x2x2(x0, l0, h0_);
-        e4m3x4_to_f16x2x2(x1, l1, h1_);
-        e4m3x4_to_f16x2x2(x2, l2, h2_);
-        e4m3x4_to_f16x2x2(x3, l3, h3_);
+        codes4_to_f16x2x2<kInt8>(x0, l0, h0_);
+        codes4_to_f16x2x2<kInt8>(x1, l1, h1_);
+        codes4_to_f16x2x2<kInt8>(x2, l2, h2_);
+        codes4_to_f16x2x2<kInt8>(x3, l3, h3_);
         l0 = hmul2_u32(l0, sclo);
         l1 = hmul2_u32(l1, sclo);
         l2 = hmul2_u32(l2, sclo);
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
   }
 }
 
-template <int NH8, int NST, bool kDual>
+template <int NH8, int NST, bool kDual, bool kInt8>
 static cudaError_t launch(const KParams& p, cudaStream_t stream) {
   using L = Layout<NH8, NST>;
   const int n_hg = (p.H + NH8 * 8 - 1) / (NH8 * 8);
@@ -431,9 +431,9 @@ static cudaError_t launch(const KParams& p, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   cudaError_t e =
-      cudaFuncSetAttribute(mma_kernel<NH8, NST, kDual>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
+      cudaFuncSetAttribute(mma_kernel<NH8, NST, kDual, kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
   if (e != cudaSuccess) return e;
-  mma_kernel<NH8, NST, kDual><<<(unsigned)grid, NT, L::total, stream>>>(p);
+  mma_kernel<NH8, NST, kDual, kInt8><<<(unsigned)grid, NT, L::total, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -442,11 +442,13 @@ static cudaError_t launch(const KParams& p, cudaStream_t stream) {
 int mma_heads_per_cta(int H) { return H <= 8 ? 8 : 16; }
 
 cudaError_t launch_mma(const KParams& p, cudaStream_t stream) {
-  if (p.dual)
-    return mma_heads_per_cta(p.H) == 8 ? mma_path::launch<1, 1, true>(p, stream)
-                                       : mma_path::launch<2, 2, true>(p, stream);
-  return mma_heads_per_cta(p.H) == 8 ? mma_path::launch<1, 1, false>(p, stream)
-                                     : mma_path::launch<2, 2, false>(p, stream);
+  using L = cudaError_t (*)(const KParams&, cudaStream_t);
+  static const L launchers[8] = {
+      mma_path::launch<1, 1, false, false>, mma_path::launch<2, 2, false, false>,
+      mma_path::launch<1, 1, true, false>,  mma_path::launch<2, 2, true, false>,
+      mma_path::launch<1, 1, false, true>,  mma_path::launch<2, 2, false, true>,
+      mma_path::launch<1, 1, true, true>,   mma_path::launch<2, 2, true, true>};
+  return launchers[(mma_heads_per_cta(p.H) == 8 ? 0 : 1) + (p.dual ? 2 : 0) + (p.kv_format == 1 ? 4 : 0)](p, stream);
 }
 
 }  // namespace smla

@@ -400,7 +400,7 @@ __device__ __forceinline__ void xreduce64(const float (&x)[64], float& r0, float
 // coalesced (4 lanes read 64 contiguous bytes of one row), and the 16 rows'
 // scale and rope chunks (9 per row) are read as 144 consecutive (row, chunk)
 // pairs.
-template <bool kEarly, bool kDual>
+template <bool kEarly, bool kDual, bool kInt8>
 __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32_t sbase, uint32_t bars, int t,
                                          int len1, int lo, int hi, int ntiles, int pw, int lane,
                                          volatile int* s_abort) {
@@ -509,10 +509,14 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
           uint32_t h[8];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n"
-                " cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
-                : "=r"(h[2 * i]), "=r"(h[2 * i + 1])
-                : "r"(w[i]));
+            if constexpr (kInt8) {
+              s8x4_to_f16x2x2(w[i], h[2 * i], h[2 * i + 1]);
+            } else {
+              asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n"
+                  " cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+                  : "=r"(h[2 * i]), "=r"(h[2 * i + 1])
+                  : "r"(w[i]));
+            }
             h[2 * i] = hmul2_u32(h[2 * i], sc2u);
             h[2 * i + 1] = hmul2_u32(h[2 * i + 1], sc2u);
           }
@@ -550,7 +554,7 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
   }
 }
 
-template <bool kEarly, bool kDual>
+template <bool kEarly, bool kDual, bool kInt8>
 __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the __shared__ array so
@@ -611,7 +615,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   if (warp < W_SOFT) {
     // ============================================================ producers
     asm volatile("setmaxnreg.inc.sync.aligned.u32 136;" ::: "memory");
-    producer<kEarly, kDual>(p, smem, sbase, bars, t, ts.len1, lo, hi, ntiles, warp, lane, s_abort);
+    producer<kEarly, kDual, kInt8>(p, smem, sbase, bars, t, ts.len1, lo, hi, ntiles, warp, lane, s_abort);
   } else if (warp >= W_MMA) {
     // ============================================================ MMA issue (warp 12; 13-15 idle)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
@@ -1013,9 +1017,14 @@ cudaError_t launch_tc(const KParams& p, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   // early row loads and L2 prefetch for a cache that does not stay in L2;
-  // the dual-cache form has its own instantiations
-  auto kern = p.dual ? (p.big_cache ? tc_path::tc_kernel<true, true> : tc_path::tc_kernel<false, true>)
-                     : (p.big_cache ? tc_path::tc_kernel<true, false> : tc_path::tc_kernel<false, false>);
+  // the dual-cache form and the int8 cache format have their own instantiations
+  using K = void (*)(const KParams);
+  static const K kerns[8] = {
+      tc_path::tc_kernel<false, false, false>, tc_path::tc_kernel<true, false, false>,
+      tc_path::tc_kernel<false, true, false>,  tc_path::tc_kernel<true, true, false>,
+      tc_path::tc_kernel<false, false, true>,  tc_path::tc_kernel<true, false, true>,
+      tc_path::tc_kernel<false, true, true>,   tc_path::tc_kernel<true, true, true>};
+  const K kern = kerns[(p.big_cache ? 1 : 0) + (p.dual ? 2 : 0) + (p.kv_format == 1 ? 4 : 0)];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_path::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)grid, tc_path::NT, tc_path::SMEM_BYTES, stream>>>(p);

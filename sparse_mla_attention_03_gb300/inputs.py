@@ -11,7 +11,8 @@ two), ``[528:656)`` 64 bf16 rope values.
 
 Recipe: nope values ``x ~ N(0,1)``; per 128-block ``scale =
 2^ceil(log2(amax/448))``; stored code = e4m3(x / scale) rounded to nearest
-even (torch's float8_e4m3fn cast); rope ``~ N(0,1)`` rounded to bf16; q ``~
+even (torch's float8_e4m3fn cast) -- or, for the int8 cache format, ``scale =
+amax/127`` and code = rint(x / scale) as a signed byte; rope ``~ N(0,1)`` rounded to bf16; q ``~
 N(0,1)`` rounded to bf16; sinks ``N(0,1)`` (or zeros); unique random indices
 per query row.  numpy PCG64, seed 0 unless stated.
 """
@@ -51,6 +52,7 @@ class Workload:
     extra_topk: int = 0
     extra_topk_length: Optional[torch.Tensor] = None  # int32 [T]
     extra_block_table: Optional[torch.Tensor] = None  # int32 [B, max_pages2]
+    kv_format: str = "e4m3"  # code bytes of every cache: "e4m3" or "int8"
 
     @property
     def dual(self):
@@ -77,8 +79,12 @@ def pow2_scale_exponent(amax: np.ndarray) -> np.ndarray:
     return np.where(v > 0, e, 0)
 
 
-def make_cache(rng: np.random.Generator, num_pages: int, chunk_rows: int = 65536) -> torch.Tensor:
-    """A paged cache ``[num_pages, 64, 656]`` of uint8 rows (see module docstring)."""
+def make_cache(rng: np.random.Generator, num_pages: int, chunk_rows: int = 65536, kv_format: str = "e4m3") -> torch.Tensor:
+    """A paged cache ``[num_pages, 64, 656]`` of uint8 rows (see module docstring).
+
+    ``kv_format="int8"``: the same row layout with signed int8 codes, per-128
+    ``scale = amax / 127`` (fp32, not a power of two) and ``code =
+    rint(x / scale)`` clipped to [-127, 127]."""
     n_rows = num_pages * PAGE
     out = np.empty((n_rows, ROW_BYTES), dtype=np.uint8)
     for lo in range(0, n_rows, chunk_rows):
@@ -86,11 +92,16 @@ def make_cache(rng: np.random.Generator, num_pages: int, chunk_rows: int = 65536
         n = hi - lo
         x = rng.standard_normal((n, 512), dtype=np.float32)
         amax = np.abs(x.reshape(n, 4, 128)).max(axis=2)
-        e = pow2_scale_exponent(amax)
-        scale = np.ldexp(np.float32(1.0), e).astype(np.float32)  # [n, 4]
-        y = (x.reshape(n, 4, 128) / scale[:, :, None]).reshape(n, 512)
-        y = np.clip(y, -448.0, 448.0)
-        codes = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        if kv_format == "int8":
+            scale = (np.maximum(amax, np.float32(1e-30)) / np.float32(127.0)).astype(np.float32)  # [n, 4]
+            y = (x.reshape(n, 4, 128) / scale[:, :, None]).reshape(n, 512)
+            codes = np.clip(np.rint(y), -127, 127).astype(np.int8).view(np.uint8)
+        else:
+            e = pow2_scale_exponent(amax)
+            scale = np.ldexp(np.float32(1.0), e).astype(np.float32)  # [n, 4]
+            y = (x.reshape(n, 4, 128) / scale[:, :, None]).reshape(n, 512)
+            y = np.clip(y, -448.0, 448.0)
+            codes = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
         rope = rng.standard_normal((n, 64), dtype=np.float32)
         rope_bits = torch.from_numpy(rope).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint8)
         out[lo:hi, 0:512] = codes
@@ -124,7 +135,7 @@ def _bf16(rng, shape):
 
 
 def make_prefill(name, T, H, ctx, topk, seed=0, sink="normal", ld=None, ragged=False,
-                 neg_prob=0.0, sm_scale=None) -> Workload:
+                 neg_prob=0.0, sm_scale=None, kv_format="e4m3") -> Workload:
     """Flat-addressed prefill: one context of ``ctx`` rows, ``topk`` unique ids per row.
 
     ``ragged``: topk_length ~ U{1..topk} per row and entries past it set to -1.
@@ -133,7 +144,7 @@ def make_prefill(name, T, H, ctx, topk, seed=0, sink="normal", ld=None, ragged=F
     """
     rng = np.random.default_rng(seed)
     assert ctx % PAGE == 0
-    kv = make_cache(rng, ctx // PAGE)
+    kv = make_cache(rng, ctx // PAGE, kv_format=kv_format)
     q = _bf16(rng, (T, H, D_QK))
     ld = topk if ld is None else ld
     idx = np.full((T, ld), POISON, dtype=np.int64)
@@ -156,12 +167,13 @@ def make_prefill(name, T, H, ctx, topk, seed=0, sink="normal", ld=None, ragged=F
     return Workload(
         name=name, q=q, kv=kv, indices=torch.from_numpy(idx.astype(np.int32)), topk=topk,
         sm_scale=(1.0 / math.sqrt(D_QK)) if sm_scale is None else sm_scale,
-        topk_length=tl, attn_sink=s,
+        topk_length=tl, attn_sink=s, kv_format=kv_format,
         meta=dict(T=T, H=H, ctx=ctx, topk=topk, ld=ld, seed=seed, ragged=ragged,
-                  neg_prob=neg_prob, sink=sink))
+                  neg_prob=neg_prob, sink=sink, kv_format=kv_format))
 
 
-def make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=0, sink="normal") -> Workload:
+def make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=0, sink="normal",
+                kv_format="e4m3") -> Workload:
     """Paged decode: ``n_req`` requests, each its own context of ``ctx_per_req``
     logical positions mapped through a block table that is one shuffled
     permutation of all pages; ``topk`` unique logical ids per query token."""
@@ -169,7 +181,7 @@ def make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=0, sink=
     assert ctx_per_req % PAGE == 0
     pages_per_req = ctx_per_req // PAGE
     num_pages = n_req * pages_per_req
-    kv = make_cache(rng, num_pages)
+    kv = make_cache(rng, num_pages, kv_format=kv_format)
     T = n_req * tokens_per_req
     q = _bf16(rng, (T, H, D_QK))
     bt = rng.permutation(num_pages).reshape(n_req, pages_per_req)
@@ -184,7 +196,7 @@ def make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=0, sink=
         name=name, q=q, kv=kv, indices=torch.from_numpy(idx.astype(np.int32)), topk=topk,
         sm_scale=1.0 / math.sqrt(D_QK), attn_sink=s,
         block_table=torch.from_numpy(bt.astype(np.int32)), tokens_per_req=tokens_per_req,
-        decode=True,
+        decode=True, kv_format=kv_format,
         meta=dict(n_req=n_req, tokens_per_req=tokens_per_req, H=H, ctx_per_req=ctx_per_req,
                   topk=topk, seed=seed, sink=sink))
 
@@ -198,15 +210,15 @@ def _ragged_lengths(rng, T, topk, idx):
 
 
 def make_dual_prefill(name, T, H, ctx, topk, extra_ctx, extra_topk, seed=0, sink="normal",
-                      ragged=False) -> Workload:
+                      ragged=False, kv_format="e4m3") -> Workload:
     """Dual-cache prefill: a flat first list of ``topk`` unique ids into a cache
     of ``ctx`` rows and a flat second list of ``extra_topk`` unique ids into a
     second cache of ``extra_ctx`` rows.  ``ragged``: both lists get
     topk_length ~ U{0..width} (so either can be empty for a token)."""
-    wl = make_prefill(name, T, H, ctx, topk, seed=seed, sink=sink)
+    wl = make_prefill(name, T, H, ctx, topk, seed=seed, sink=sink, kv_format=kv_format)
     rng = np.random.default_rng(seed + 7919)
     assert extra_ctx % PAGE == 0
-    wl.extra_kv = make_cache(rng, extra_ctx // PAGE)
+    wl.extra_kv = make_cache(rng, extra_ctx // PAGE, kv_format=kv_format)
     idx2 = unique_rows(rng, T, extra_topk, extra_ctx)
     if ragged:
         idx1 = wl.indices.numpy().astype(np.int64)
@@ -220,15 +232,15 @@ def make_dual_prefill(name, T, H, ctx, topk, extra_ctx, extra_topk, seed=0, sink
 
 
 def make_dual_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, extra_ctx_per_req, extra_topk,
-                     seed=0, sink="normal") -> Workload:
+                     seed=0, sink="normal", kv_format="e4m3") -> Workload:
     """Dual-cache decode: the paged decode of ``make_decode`` plus, per
     request, a second paged cache of ``extra_ctx_per_req`` logical positions
     (its own shuffled block table) and ``extra_topk`` unique logical ids."""
-    wl = make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=seed, sink=sink)
+    wl = make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=seed, sink=sink, kv_format=kv_format)
     rng = np.random.default_rng(seed + 7919)
     assert extra_ctx_per_req % PAGE == 0
     pages2 = extra_ctx_per_req // PAGE
-    wl.extra_kv = make_cache(rng, n_req * pages2)
+    wl.extra_kv = make_cache(rng, n_req * pages2, kv_format=kv_format)
     wl.extra_block_table = torch.from_numpy(rng.permutation(n_req * pages2).reshape(n_req, pages2).astype(np.int32))
     wl.extra_indices = torch.from_numpy(unique_rows(rng, wl.T, extra_topk, extra_ctx_per_req).astype(np.int32))
     wl.extra_topk = extra_topk
@@ -271,6 +283,13 @@ def dual_decode(seed=0, n_req=64):
                             extra_topk=2176, seed=seed)
 
 
+def prefill_16k_int8(topk=1024, seed=0, T=1024):
+    """The 16k-footprint prefill on an INT8 cache (the AppMana releases page
+    times "int8 width 1024" at this footprint)."""
+    return make_prefill(f"prefill_T{T}_H64_ctx16384_k{topk}_int8", T=T, H=64, ctx=16384, topk=topk, seed=seed,
+                        kv_format="int8")
+
+
 WORKLOADS = {
     "tiny": tiny_prefill,
     "prefill16k_k512": lambda seed=0: prefill_16k(512, seed),
@@ -279,4 +298,5 @@ WORKLOADS = {
     "decode": batched_decode,
     "large": large_prefill,
     "dual_decode": dual_decode,
+    "prefill16k_int8": prefill_16k_int8,
 }

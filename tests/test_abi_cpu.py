@@ -55,7 +55,7 @@ def _args(**kw):
 @pytest.mark.parametrize("bad", [
     dict(H=0), dict(H=129), dict(topk=0), dict(T=-1), dict(q_stride_t=100), dict(out_stride_t=8 * 512 + 2),
     dict(lse_stride_t=4), dict(idx_stride_t=10), dict(q=0), dict(kv=0x2001), dict(out=0x4002),
-    dict(reserved0=1), dict(sm_scale=float("nan")), dict(num_pages=-1),
+    dict(kv_format=2), dict(sm_scale=float("nan")), dict(num_pages=-1),
     dict(block_table=0x6000, bt_rows=1, bt_cols=8, bt_stride=8, tokens_per_req=2),  # 2 tokens/row x 1 row < 4
     dict(block_table=0x6000, bt_rows=4, bt_cols=8, bt_stride=4, tokens_per_req=1),  # stride < cols
 ])
@@ -90,4 +90,4 @@ def test_explicit_split_arithmetic(lib):
     assert lib.sparse_mla_decode_num_splits(4, 8, 640, 3) == 3
     ws = lib.sparse_mla_decode_workspace_size(128, 64, 2048, 8)
     assert ws == 128 * 64 * 8 * 512 * 4 + 128 * 64 * 8 * 4
-    assert lib.sparse_mla_abi_version() == 2
+    assert lib.sparse_mla_abi_version() == 3

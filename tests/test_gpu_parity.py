@@ -19,7 +19,8 @@ def run_prefill(wl, **kw):
     d = to_dev(wl)
     return binding.sparse_mla_prefill(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
                                       topk_length=d["topk_length"], attn_sink=d["attn_sink"],
-                                      block_table=d["block_table"], tokens_per_req=wl.tokens_per_req, **kw)
+                                      block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
+                                      kv_format=wl.kv_format, **kw)
 
 
 def run_decode(wl, num_splits=0, **kw):
@@ -27,7 +28,7 @@ def run_decode(wl, num_splits=0, **kw):
     return binding.sparse_mla_decode(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
                                      topk_length=d["topk_length"], attn_sink=d["attn_sink"],
                                      block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
-                                     num_splits=num_splits, **kw)
+                                     num_splits=num_splits, kv_format=wl.kv_format, **kw)
 
 
 @pytest.fixture(autouse=True)
@@ -196,7 +197,7 @@ def run_dual(wl, decode=False, num_splits=0):
     d = to_dev(wl)
     kw = dict(topk=wl.topk, topk_length=d["topk_length"], extra_topk=wl.extra_topk,
               extra_topk_length=d["extra_topk_length"], attn_sink=d["attn_sink"], block_table=d["block_table"],
-              extra_block_table=d["extra_block_table"], tokens_per_req=wl.tokens_per_req)
+              extra_block_table=d["extra_block_table"], tokens_per_req=wl.tokens_per_req, kv_format=wl.kv_format)
     if decode:
         return binding.sparse_mla_decode_dual(d["q"], d["kv"], d["indices"], d["extra_kv"], d["extra_indices"],
                                               wl.sm_scale, num_splits=num_splits, **kw)
@@ -289,6 +290,43 @@ def test_dual_rejects_bad_extra():
                                         wl.sm_scale, extra_topk=0)
 
 
+# ----------------------------------------------------------------------------- int8 cache format
+@pytest.mark.parametrize("H", [1, 8, 16, 64, 128])
+def test_int8_prefill_ragged(H):
+    wl = inputs.make_prefill("i8p", T=6, H=H, ctx=2048, topk=300, seed=201 + H, ragged=True, kv_format="int8")
+    out, lse = run_prefill(wl)
+    assert_close(out, lse, *oracle_for(wl), tag=f"int8_prefill_H{H}")
+    assert binding.get_error_word() == 0
+
+
+@pytest.mark.parametrize("H,S", [(64, 0), (64, 3), (8, 0), (8, 4)])
+def test_int8_decode_paged(H, S):
+    wl = inputs.make_decode("i8d", n_req=3, tokens_per_req=2, H=H, ctx_per_req=4096, topk=512, seed=211 + S,
+                            kv_format="int8")
+    out, lse = run_decode(wl, num_splits=S)
+    assert_close(out, lse, *oracle_for(wl), tag=f"int8_decode_H{H}_S{S}")
+    assert binding.get_error_word() == 0
+
+
+def test_int8_dual_and_beyond_l2():
+    wl = inputs.make_dual_prefill("i8dual", T=4, H=64, ctx=65536, topk=320, extra_ctx=2048, extra_topk=200,
+                                  seed=221, ragged=True, kv_format="int8")
+    out, lse = run_dual(wl)
+    assert_close(out, lse, *oracle_dual_for(wl), tag="int8_dual_bigcache")
+    assert binding.get_error_word() == 0
+
+
+def test_int8_differs_from_e4m3_reading():
+    # the same bytes read in the two formats give different results: the
+    # format field reaches the kernels
+    wl = inputs.make_prefill("i8fmt", T=2, H=8, ctx=256, topk=64, seed=231, kv_format="int8")
+    a, _ = run_prefill(wl)
+    wl.kv_format = "e4m3"
+    b, _ = run_prefill(wl)
+    diff = (a.float() - b.float()).abs()  # codes 0x7F / 0xFF are NaN when read as e4m3
+    assert torch.isnan(diff).any() or diff.max().item() > 1e-2
+
+
 # ----------------------------------------------------------------------------- full-size workloads
 FULL = {
     "prefill16k_k512": (lambda: inputs.prefill_16k(512), "prefill", 48),
@@ -297,6 +335,7 @@ FULL = {
     "decode": (inputs.batched_decode, "decode", 48),
     "large": (inputs.large_prefill, "prefill", 24),
     "dual_decode": (inputs.dual_decode, "dual_decode", 32),
+    "prefill16k_int8_k1024": (inputs.prefill_16k_int8, "prefill", 32),
 }
 
 

@@ -479,3 +479,61 @@ def test_dual_cache_planted_mistakes_are_caught():
     for bad in (second_list_in_first_cache, two_softmaxes_averaged, second_length_ignored):
         with pytest.raises(AssertionError):
             check_dual(bad)
+
+
+# ----------------------------------------------------------------------------- int8 cache format
+def dequant_int8_via_torch(kv_rows):
+    """int8 codes through torch's own int8 view (independent of the oracle)."""
+    t = torch.from_numpy(np.ascontiguousarray(kv_rows))
+    codes = t[:, :512].contiguous().view(torch.int8).to(torch.float64)
+    sc = t[:, 512:528].contiguous().view(torch.float32).to(torch.float64)
+    rope = t[:, 528:656].contiguous().view(torch.bfloat16).to(torch.float64)
+    return torch.cat([codes * sc.repeat_interleave(128, dim=1), rope], dim=1)
+
+
+def check_int8(int8_to_f64=O.int8_to_f64, decode_rows=O.decode_rows):
+    codes = np.arange(256, dtype=np.uint8)
+    ours = int8_to_f64(codes)
+    lib = torch.from_numpy(codes).view(torch.int8).to(torch.float64).numpy()
+    assert np.array_equal(ours, lib)
+    assert ours[0x7F] == 127 and ours[0x80] == -128 and ours[0xFF] == -1 and ours[0x01] == 1
+    wl = inputs.make_prefill("dq8", T=1, H=1, ctx=128, topk=8, seed=11, kv_format="int8")
+    rows = wl.kv.numpy().reshape(-1, 656)
+    assert np.array_equal(decode_rows(rows, "int8"), dequant_int8_via_torch(rows).numpy())
+    # by hand: code 0xFE (-2) at nope[300] with scale[2] = 0.75 -> -1.5
+    r = build_row({300: 0xFE}, scales=(1.0, 1.0, 0.75, 1.0))
+    k = decode_rows(r[None, :], "int8")[0]
+    assert k[300] == -1.5 and np.count_nonzero(k) == 1
+
+
+def test_int8_decoder_and_rows():
+    check_int8()
+
+
+def test_int8_dense_coverage_equals_sdpa():
+    rng = np.random.default_rng(9)
+    wl = inputs.make_prefill("dense8", T=3, H=4, ctx=256, topk=256, seed=9, sink=None, kv_format="int8")
+    wl.indices = torch.from_numpy(np.stack([rng.permutation(256) for _ in range(3)]).astype(np.int32))
+    sink = np.array([0.3, -1.2, 2.0, 0.0])
+    out, lse = O.sparse_mla_forward(q_f64(wl), wl.kv.numpy(), wl.indices.numpy(), 256, wl.sm_scale,
+                                    attn_sink=sink, kv_format="int8")
+    K = dequant_int8_via_torch(wl.kv.numpy().reshape(-1, 656)).numpy()
+    for t in range(wl.T):
+        ro, rl = sdpa_dense(q_f64(wl)[t], K, wl.sm_scale, sink)
+        np.testing.assert_allclose(out[t], ro, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[t], rl, rtol=0, atol=1e-12)
+
+
+def test_int8_planted_mistakes_are_caught():
+    def unsigned(codes):
+        return np.asarray(codes, dtype=np.uint8).astype(np.float64)
+
+    def offset_binary(codes):
+        return np.asarray(codes, dtype=np.uint8).astype(np.float64) - 128.0
+
+    for bad in (unsigned, offset_binary):
+        with pytest.raises(AssertionError):
+            check_int8(int8_to_f64=bad)
+    # the row decoder reading int8 rows as e4m3 fails the row pin
+    with pytest.raises(AssertionError):
+        check_int8(decode_rows=lambda rows, fmt: O.decode_rows(rows, "e4m3"))
