@@ -128,15 +128,15 @@ def load_peaks():
 def _oracle_chunk(args):
     import numpy as np
     import oracle.sparse_mla_oracle as O
-    (q, kv, idx, topk, sm, tl, sink, bt, tpr, toks, extra, fmt) = args
+    (q, kv, idx, topk, sm, tl, sink, bt, tpr, toks, extra, fmt, layout) = args
     if extra is None:
         O.sparse_mla_forward(q, kv, idx, topk, sm, topk_length=tl, attn_sink=sink, block_table=bt,
-                             tokens_per_req=tpr, tokens=toks, q_selected=True, kv_format=fmt)
+                             tokens_per_req=tpr, tokens=toks, q_selected=True, kv_format=fmt, layout=layout)
     else:
         kv2, idx2, topk2, tl2, bt2 = extra
         O.sparse_mla_forward_dual(q, kv, idx, topk, kv2, idx2, topk2, sm, topk_length=tl, extra_topk_length=tl2,
                                   attn_sink=sink, block_table=bt, extra_block_table=bt2, tokens_per_req=tpr,
-                                  tokens=toks, q_selected=True, kv_format=fmt)
+                                  tokens=toks, q_selected=True, kv_format=fmt, layout=layout)
     return len(toks)
 
 
@@ -156,7 +156,7 @@ def oracle_time(wl, n_tokens, cores, pool=None):
     extra = (wl.extra_kv.numpy(), wl.extra_indices.numpy(), wl.extra_topk, np_(wl.extra_topk_length),
              np_(wl.extra_block_table)) if wl.dual else None
     jobs = [(wl.q[torch.as_tensor(c)].to(torch.float64).numpy(), kv, idx, wl.topk, wl.sm_scale, tl, sink, bt,
-             wl.tokens_per_req, c, extra, wl.kv_format) for c in chunks]
+             wl.tokens_per_req, c, extra, wl.kv_format, wl.layout) for c in chunks]
     own = pool is None
     if own:
         pool = mp.get_context("spawn").Pool(cores, initializer=_pin_threads)
@@ -265,14 +265,14 @@ def make_call(kind, binding, d, wl, out, lse, ws, num_splits):
             binding.sparse_mla_prefill(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
                                        topk_length=d["topk_length"], attn_sink=d["attn_sink"],
                                        block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
-                                       out=out, lse=lse, stream=stream, kv_format=wl.kv_format)
+                                       out=out, lse=lse, stream=stream, kv_format=wl.kv_format, layout=wl.layout)
     elif kind == "decode":
         def call(stream=None):
             binding.sparse_mla_decode(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
                                       topk_length=d["topk_length"], attn_sink=d["attn_sink"],
                                       block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
                                       num_splits=num_splits, workspace=ws, out=out, lse=lse, stream=stream,
-                                      kv_format=wl.kv_format)
+                                      kv_format=wl.kv_format, layout=wl.layout)
     else:
         def call(stream=None):
             binding.sparse_mla_decode_dual(d["q"], d["kv"], d["indices"], d["extra_kv"], d["extra_indices"],
@@ -281,7 +281,7 @@ def make_call(kind, binding, d, wl, out, lse, ws, num_splits):
                                            attn_sink=d["attn_sink"], block_table=d["block_table"],
                                            extra_block_table=d["extra_block_table"],
                                            tokens_per_req=wl.tokens_per_req, num_splits=num_splits, workspace=ws,
-                                           out=out, lse=lse, stream=stream, kv_format=wl.kv_format)
+                                           out=out, lse=lse, stream=stream, kv_format=wl.kv_format, layout=wl.layout)
     return call
 
 

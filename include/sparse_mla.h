@@ -103,11 +103,27 @@ enum {
 #define SMLA_KV_INT8 1
 
 /*
+ * Row layouts (FlashInfer PR #4802, review note on the KV layout comment of
+ * the DSv3.2 decode kernel):
+ *  SMLA_LAYOUT_ROPE64  [528, 656) holds 64 bf16 rope values; d_qk = 576 and
+ *                      q is [T, H, 576] (head stride 576).
+ *  SMLA_LAYOUT_NOPE    GLM53_NOPE: the same 656-byte row with d_rope = 0;
+ *                      [528, 656) is reserved padding and is never read;
+ *                      d_qk = 512 and q is [T, H, 512] (head stride 512).
+ * GLM_NSA's arbitrary (not power-of-two) fp32 scales need no flag: every
+ * scale is taken as stored (rounded to fp16 by the kernels).
+ */
+#define SMLA_LAYOUT_ROPE64 0
+#define SMLA_LAYOUT_NOPE 1
+
+/*
  * Arguments shared by prefill and decode.  Strides are in ELEMENTS of the
  * pointed-to type.
  *
  *  q            bf16 [T, H, 576]: head stride 576, token stride q_stride_t
- *               (>= H*576; a view into a wider buffer is fine).
+ *               (>= H*576; a view into a wider buffer is fine).  With
+ *               SMLA_LAYOUT_NOPE: [T, H, 512], head stride 512, q_stride_t
+ *               >= H*512.
  *  kv           uint8 [num_pages, 64, 656], contiguous rows, 16-byte aligned.
  *  block_table  int32 [bt_rows, >= bt_cols] with row stride bt_stride, or
  *               NULL for flat row ids.  tokens_per_req query tokens share a
@@ -121,6 +137,8 @@ enum {
  *               (>= H*512, multiple of 4), 8-byte aligned; written in place.
  *  lse          fp32 [T, H]: token stride lse_stride_t (>= H).
  *  kv_format    SMLA_KV_E4M3 or SMLA_KV_INT8 (see above).
+ *  layout       SMLA_LAYOUT_ROPE64 or SMLA_LAYOUT_NOPE (see above); both
+ *               caches of a dual call share it.  reserved1 must be 0.
  *  H in [1, 128]; T >= 0; topk >= 1.
  */
 typedef struct smla_args {
@@ -146,6 +164,8 @@ typedef struct smla_args {
   int64_t out_stride_t;
   float* lse;
   int64_t lse_stride_t;
+  int32_t layout;
+  int32_t reserved1;
 } smla_args;
 
 /*

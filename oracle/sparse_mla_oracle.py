@@ -112,7 +112,7 @@ def f32_le_bytes_to_f64(b: np.ndarray) -> np.ndarray:
 # ----------------------------------------------------------------------------
 # Row decoding (the dequantisation step)
 # ----------------------------------------------------------------------------
-def decode_rows(rows: np.ndarray, kv_format: str = "e4m3") -> np.ndarray:
+def decode_rows(rows: np.ndarray, kv_format: str = "e4m3", layout: str = "rope64") -> np.ndarray:
     """Dequantise latent rows: uint8 ``[n, 656]`` -> float64 ``[n, 576]``.
 
     ``k[i] = code(byte[i]) * scale[i // 128]`` for ``i < 512`` and
@@ -120,7 +120,9 @@ def decode_rows(rows: np.ndarray, kv_format: str = "e4m3") -> np.ndarray:
     layout note).  V of the same row is ``k[:512]``.  ``code`` is e4m3, or
     for ``kv_format="int8"`` a signed byte: the AppMana releases page names
     INT8 latent-cache kernels without a byte layout, read here as the same
-    row with int8 codes in place of e4m3.
+    row with int8 codes in place of e4m3.  ``layout="nope"`` (GLM53_NOPE,
+    FlashInfer PR #4802 review note on the KV layout comment): no rope,
+    ``[528:656)`` is padding and is not read; the result is ``[n, 512]``.
     """
     rows = np.asarray(rows, dtype=np.uint8)
     assert rows.ndim == 2 and rows.shape[1] == ROW_BYTES, rows.shape
@@ -129,6 +131,9 @@ def decode_rows(rows: np.ndarray, kv_format: str = "e4m3") -> np.ndarray:
     nope = (int8_to_f64 if kv_format == "int8" else e4m3_to_f64)(rows[:, :D_NOPE])
     scales = f32_le_bytes_to_f64(rows[:, _SCALE_OFF:_ROPE_OFF]).reshape(n, D_NOPE // SCALE_BLOCK)
     nope = nope * np.repeat(scales, SCALE_BLOCK, axis=1)
+    if layout == "nope":
+        return nope
+    assert layout == "rope64", layout
     rope_bits = np.ascontiguousarray(rows[:, _ROPE_OFF:ROW_BYTES]).view("<u2")
     rope = bf16_bits_to_f64(rope_bits)
     return np.concatenate([nope, rope], axis=1)
@@ -181,7 +186,7 @@ def resolve_rows(indices, topk, num_pages, topk_length=None, block_table=None,
 def attend_one(q_t, K, sm_scale, sink=None):
     """Sink softmax attention of one token over its gathered rows.
 
-    ``q_t``: ``[H, 576]`` float64; ``K``: ``[n, 576]`` dequantised rows
+    ``q_t``: ``[H, d_qk]`` float64; ``K``: ``[n, d_qk]`` dequantised rows
     (``V = K[:, :512]``); ``sink``: ``[H]`` logits or None.
     Returns ``(out [H, 512], lse [H])`` with
 
@@ -204,7 +209,7 @@ def attend_one(q_t, K, sm_scale, sink=None):
 
 def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
                        attn_sink=None, block_table=None, tokens_per_req=1,
-                       tokens=None, q_selected=False, kv_format="e4m3"):
+                       tokens=None, q_selected=False, kv_format="e4m3", layout="rope64"):
     """Sparse MLA forward for the selected tokens (all tokens by default).
 
     ``q``: float64 ``[T, H, 576]`` (bf16 values widened exactly), or only the
@@ -218,7 +223,7 @@ def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
     q = np.asarray(q, dtype=np.float64)
     T = np.asarray(indices).shape[0]
     _, H, D = q.shape
-    assert D == D_QK
+    assert D == (D_QK if layout == "rope64" else D_NOPE)
     sel = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     if q_selected:
         assert q.shape[0] == sel.shape[0]
@@ -229,7 +234,7 @@ def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
     sink = None if attn_sink is None else np.asarray(attn_sink, dtype=np.float64)
     for i, t in enumerate(sel):
         r = rows[i]
-        K = decode_rows(kv[r[r >= 0]], kv_format)
+        K = decode_rows(kv[r[r >= 0]], kv_format, layout)
         out[i], lse[i] = attend_one(q[i] if q_selected else q[t], K, sm_scale, sink)
     return out, lse
 
@@ -237,7 +242,7 @@ def sparse_mla_forward(q, kv_cache, indices, topk, sm_scale, topk_length=None,
 def sparse_mla_forward_dual(q, kv_cache, indices, topk, extra_kv_cache, extra_indices, extra_topk,
                             sm_scale, topk_length=None, extra_topk_length=None, attn_sink=None,
                             block_table=None, extra_block_table=None, tokens_per_req=1,
-                            tokens=None, q_selected=False, kv_format="e4m3"):
+                            tokens=None, q_selected=False, kv_format="e4m3", layout="rope64"):
     """Dual-cache form: one sink softmax per token over the valid slots of two
     index lists, the first resolved in ``kv_cache`` and the second in
     ``extra_kv_cache`` (FlashInfer PR #4802: the DSv4 secondary cache with its
@@ -254,7 +259,7 @@ def sparse_mla_forward_dual(q, kv_cache, indices, topk, extra_kv_cache, extra_in
     q = np.asarray(q, dtype=np.float64)
     T = np.asarray(indices).shape[0]
     _, H, D = q.shape
-    assert D == D_QK and np.asarray(extra_indices).shape[0] == T
+    assert D == (D_QK if layout == "rope64" else D_NOPE) and np.asarray(extra_indices).shape[0] == T
     sel = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     if q_selected:
         assert q.shape[0] == sel.shape[0]
@@ -267,8 +272,8 @@ def sparse_mla_forward_dual(q, kv_cache, indices, topk, extra_kv_cache, extra_in
     sink = None if attn_sink is None else np.asarray(attn_sink, dtype=np.float64)
     for i, t in enumerate(sel):
         r1, r2 = rows1[i], rows2[i]
-        K = np.concatenate([decode_rows(kv1[r1[r1 >= 0]], kv_format), decode_rows(kv2[r2[r2 >= 0]], kv_format)],
-                           axis=0)
+        K = np.concatenate([decode_rows(kv1[r1[r1 >= 0]], kv_format, layout),
+                            decode_rows(kv2[r2[r2 >= 0]], kv_format, layout)], axis=0)
         out[i], lse[i] = attend_one(q[i] if q_selected else q[t], K, sm_scale, sink)
     return out, lse
 

@@ -22,6 +22,7 @@ D_QK, D_V, ROW_BYTES, PAGE = 576, 512, 656, 64
 
 SMLA_OK, SMLA_ERR_INVALID, SMLA_ERR_UNSUPPORTED, SMLA_ERR_CUDA, SMLA_ERR_DEVICE = range(5)
 KV_FORMATS = {"e4m3": 0, "int8": 1}  # SMLA_KV_E4M3, SMLA_KV_INT8
+LAYOUTS = {"rope64": 0, "nope": 1}  # SMLA_LAYOUT_ROPE64, SMLA_LAYOUT_NOPE
 ERRF_INDEX_RANGE, ERRF_TIMEOUT, ERRF_SCALE_RANGE = 1, 2, 4
 
 
@@ -44,6 +45,7 @@ class SmlaArgs(ctypes.Structure):
         ("kv_format", ctypes.c_int32),
         ("out", ctypes.c_void_p), ("out_stride_t", ctypes.c_int64),
         ("lse", ctypes.c_void_p), ("lse_stride_t", ctypes.c_int64),
+        ("layout", ctypes.c_int32), ("reserved1", ctypes.c_int32),
     ]
 
 
@@ -119,7 +121,7 @@ def _stream_handle(stream):
 
 
 def make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length=None, attn_sink=None,
-              block_table=None, tokens_per_req=1, kv_format="e4m3") -> SmlaArgs:
+              block_table=None, tokens_per_req=1, kv_format="e4m3", layout="rope64") -> SmlaArgs:
     """Validate tensor layouts and build the C struct (no data is touched)."""
     T, H = q.shape[0], q.shape[1]
     dev = q.device
@@ -140,8 +142,11 @@ def make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length=None, attn_s
     on_dev(topk_length, "topk_length", torch.int32)
     on_dev(attn_sink, "attn_sink", torch.float32)
     on_dev(block_table, "block_table", torch.int32)
-    if q.dim() != 3 or q.shape[2] != D_QK or q.stride(2) != 1 or q.stride(1) != D_QK:
-        raise ValueError("q must be [T, H, 576] with head stride 576 and unit last stride")
+    if layout not in LAYOUTS:
+        raise ValueError(f"layout must be one of {sorted(LAYOUTS)}, got {layout!r}")
+    d_qk = D_QK if layout == "rope64" else D_V
+    if q.dim() != 3 or q.shape[2] != d_qk or q.stride(2) != 1 or q.stride(1) != d_qk:
+        raise ValueError(f"q must be [T, H, {d_qk}] with head stride {d_qk} and unit last stride")
     if kv.dim() != 3 or tuple(kv.shape[1:]) != (PAGE, ROW_BYTES) or not kv.is_contiguous():
         raise ValueError("kv must be a contiguous [num_pages, 64, 656] uint8 tensor")
     if indices.dim() != 2 or indices.shape[0] != T or indices.stride(1) != 1 or indices.shape[1] < topk:
@@ -175,6 +180,7 @@ def make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length=None, attn_s
     if kv_format not in KV_FORMATS:
         raise ValueError(f"kv_format must be one of {sorted(KV_FORMATS)}, got {kv_format!r}")
     a.kv_format = KV_FORMATS[kv_format]
+    a.layout = LAYOUTS[layout]
     return a
 
 
@@ -188,13 +194,14 @@ def _outputs(q, out, lse):
 
 
 def sparse_mla_prefill(q, kv, indices, sm_scale, topk=None, topk_length=None, attn_sink=None,
-                       block_table=None, tokens_per_req=1, out=None, lse=None, stream=None, kv_format="e4m3"):
+                       block_table=None, tokens_per_req=1, out=None, lse=None, stream=None,
+                       kv_format="e4m3", layout="rope64"):
     """Sparse MLA prefill; returns ``(out bf16 [T,H,512], lse fp32 [T,H])``."""
     lib = load()
     topk = indices.shape[1] if topk is None else topk
     out, lse = _outputs(q, out, lse)
     a = make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length, attn_sink, block_table,
-                  tokens_per_req, kv_format)
+                  tokens_per_req, kv_format, layout)
     _check(lib.sparse_mla_prefill(ctypes.byref(a), _stream_handle(stream)))
     return out, lse
 
@@ -209,7 +216,8 @@ def decode_num_splits(T, H, topk, num_splits=0) -> int:
 
 def sparse_mla_decode(q, kv, indices, sm_scale, topk=None, topk_length=None, attn_sink=None,
                       block_table=None, tokens_per_req=1, num_splits=0, workspace=None, out=None,
-                      lse=None, stream=None, kv_format="e4m3"):
+                      lse=None, stream=None,
+                       kv_format="e4m3", layout="rope64"):
     """Split-K sparse MLA decode plus combine; returns ``(out, lse)``.
 
     ``workspace``: a uint8 CUDA tensor of at least ``decode_workspace_size``
@@ -218,7 +226,7 @@ def sparse_mla_decode(q, kv, indices, sm_scale, topk=None, topk_length=None, att
     topk = indices.shape[1] if topk is None else topk
     out, lse = _outputs(q, out, lse)
     a = make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length, attn_sink, block_table,
-                  tokens_per_req, kv_format)
+                  tokens_per_req, kv_format, layout)
     need = decode_workspace_size(q.shape[0], q.shape[1], topk, num_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -232,7 +240,8 @@ NOALLOC_SCRATCH_BYTES = 64 << 20
 
 def sparse_mla_decode_noalloc(q, kv, indices, sm_scale, topk=None, topk_length=None, attn_sink=None,
                               block_table=None, tokens_per_req=1, num_splits=0, out=None, lse=None,
-                              stream=None, kv_format="e4m3"):
+                              stream=None,
+                       kv_format="e4m3", layout="rope64"):
     """Split-K decode whose partials live in the library's built-in scratch
     array: for callers that cannot allocate device memory.  ``out``/``lse``
     must be passed to allocate nothing here either."""
@@ -240,21 +249,23 @@ def sparse_mla_decode_noalloc(q, kv, indices, sm_scale, topk=None, topk_length=N
     topk = indices.shape[1] if topk is None else topk
     out, lse = _outputs(q, out, lse)
     a = make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length, attn_sink, block_table,
-                  tokens_per_req, kv_format)
+                  tokens_per_req, kv_format, layout)
     _check(lib.sparse_mla_decode_noalloc(ctypes.byref(a), int(num_splits), _stream_handle(stream)))
     return out, lse
 
 
 def sparse_mla_resolve_rows(q, kv, indices, topk=None, topk_length=None, block_table=None,
-                            tokens_per_req=1, stream=None, kv_format="e4m3"):
+                            tokens_per_req=1, stream=None,
+                       kv_format="e4m3", layout="rope64"):
     """Physical cache row per slot (int32 [T, topk], -1 = invalid), from the device."""
     lib = load()
     topk = indices.shape[1] if topk is None else topk
     T, H = q.shape[0], q.shape[1]
-    out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=q.device) if T else torch.empty(0, H, D_V, dtype=torch.bfloat16, device=q.device)
+    out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
     rows = torch.empty((T, topk), dtype=torch.int32, device=q.device)
-    a = make_args(q, kv, indices, topk, 1.0, out, lse, topk_length, None, block_table, tokens_per_req, kv_format)
+    a = make_args(q, kv, indices, topk, 1.0, out, lse, topk_length, None, block_table, tokens_per_req,
+                  kv_format, layout)
     _check(lib.sparse_mla_resolve_rows(ctypes.byref(a), rows.data_ptr(), topk, _stream_handle(stream)))
     return rows
 
@@ -307,13 +318,14 @@ def dual_width(topk, extra_topk) -> int:
 
 def sparse_mla_prefill_dual(q, kv, indices, extra_kv, extra_indices, sm_scale, topk=None, topk_length=None,
                             extra_topk=None, extra_topk_length=None, attn_sink=None, block_table=None,
-                            extra_block_table=None, tokens_per_req=1, out=None, lse=None, stream=None, kv_format="e4m3"):
+                            extra_block_table=None, tokens_per_req=1, out=None, lse=None, stream=None,
+                       kv_format="e4m3", layout="rope64"):
     """One softmax over two index lists into two caches; returns ``(out, lse)``."""
     lib = load()
     topk = indices.shape[1] if topk is None else topk
     out, lse = _outputs(q, out, lse)
     a = make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length, attn_sink, block_table,
-                  tokens_per_req, kv_format)
+                  tokens_per_req, kv_format, layout)
     a.tokens_per_req = int(tokens_per_req)
     x = make_extra(q, extra_kv, extra_indices, extra_topk, extra_topk_length, extra_block_table)
     _check(lib.sparse_mla_prefill_dual(ctypes.byref(a), ctypes.byref(x), _stream_handle(stream)))
@@ -323,13 +335,14 @@ def sparse_mla_prefill_dual(q, kv, indices, extra_kv, extra_indices, sm_scale, t
 def sparse_mla_decode_dual(q, kv, indices, extra_kv, extra_indices, sm_scale, topk=None, topk_length=None,
                            extra_topk=None, extra_topk_length=None, attn_sink=None, block_table=None,
                            extra_block_table=None, tokens_per_req=1, num_splits=0, workspace=None,
-                           out=None, lse=None, stream=None, kv_format="e4m3"):
+                           out=None, lse=None, stream=None,
+                       kv_format="e4m3", layout="rope64"):
     """Split-K decode of the dual-cache form plus combine; returns ``(out, lse)``."""
     lib = load()
     topk = indices.shape[1] if topk is None else topk
     out, lse = _outputs(q, out, lse)
     a = make_args(q, kv, indices, topk, sm_scale, out, lse, topk_length, attn_sink, block_table,
-                  tokens_per_req, kv_format)
+                  tokens_per_req, kv_format, layout)
     a.tokens_per_req = int(tokens_per_req)
     x = make_extra(q, extra_kv, extra_indices, extra_topk, extra_topk_length, extra_block_table)
     need = decode_workspace_size(q.shape[0], q.shape[1], dual_width(topk, x.topk), num_splits)
@@ -342,7 +355,8 @@ def sparse_mla_decode_dual(q, kv, indices, extra_kv, extra_indices, sm_scale, to
 
 def sparse_mla_resolve_rows_dual(q, kv, indices, extra_kv, extra_indices, topk=None, topk_length=None,
                                  extra_topk=None, extra_topk_length=None, block_table=None,
-                                 extra_block_table=None, tokens_per_req=1, stream=None, kv_format="e4m3"):
+                                 extra_block_table=None, tokens_per_req=1, stream=None,
+                       kv_format="e4m3", layout="rope64"):
     """Row per combined slot (int32 [T, width]); second-cache rows are offset
     by the first cache's row count; -1 = invalid or padding."""
     lib = load()
@@ -350,7 +364,8 @@ def sparse_mla_resolve_rows_dual(q, kv, indices, extra_kv, extra_indices, topk=N
     T, H = q.shape[0], q.shape[1]
     out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
-    a = make_args(q, kv, indices, topk, 1.0, out, lse, topk_length, None, block_table, tokens_per_req, kv_format)
+    a = make_args(q, kv, indices, topk, 1.0, out, lse, topk_length, None, block_table, tokens_per_req,
+                  kv_format, layout)
     a.tokens_per_req = int(tokens_per_req)
     x = make_extra(q, extra_kv, extra_indices, extra_topk, extra_topk_length, extra_block_table)
     width = dual_width(topk, x.topk)

@@ -61,6 +61,9 @@ int validate(const smla_args* a) {
   if (a->topk < 1) return fail(SMLA_ERR_INVALID, "topk = %d < 1", a->topk);
   if (a->kv_format != SMLA_KV_E4M3 && a->kv_format != SMLA_KV_INT8)
     return fail(SMLA_ERR_INVALID, "kv_format = %d is neither SMLA_KV_E4M3 nor SMLA_KV_INT8", a->kv_format);
+  if (a->layout != SMLA_LAYOUT_ROPE64 && a->layout != SMLA_LAYOUT_NOPE)
+    return fail(SMLA_ERR_INVALID, "layout = %d is neither SMLA_LAYOUT_ROPE64 nor SMLA_LAYOUT_NOPE", a->layout);
+  if (a->reserved1 != 0) return fail(SMLA_ERR_INVALID, "reserved1 must be 0");
   if (!(a->sm_scale == a->sm_scale) || a->sm_scale > 3.0e38f || a->sm_scale < -3.0e38f)
     return fail(SMLA_ERR_INVALID, "sm_scale is not finite");
   if (a->T == 0) return SMLA_OK;
@@ -70,8 +73,8 @@ int validate(const smla_args* a) {
     return fail(SMLA_ERR_INVALID, "num_pages = %lld out of range", (long long)a->num_pages);
   if (a->num_pages > 0 && !a->kv) return fail(SMLA_ERR_INVALID, "kv is NULL");
   if (a->kv && !aligned(a->kv, 16)) return fail(SMLA_ERR_INVALID, "kv must be 16-byte aligned");
-  if (a->q_stride_t < (int64_t)a->H * SMLA_D_QK)
-    return fail(SMLA_ERR_INVALID, "q_stride_t = %lld < H*576", (long long)a->q_stride_t);
+  if (a->q_stride_t < (int64_t)a->H * (a->layout == SMLA_LAYOUT_NOPE ? 512 : SMLA_D_QK))
+    return fail(SMLA_ERR_INVALID, "q_stride_t = %lld < H*d_qk", (long long)a->q_stride_t);
   if (a->out_stride_t < (int64_t)a->H * SMLA_D_V || a->out_stride_t % 4 != 0)
     return fail(SMLA_ERR_INVALID, "out_stride_t = %lld must be >= H*512 and a multiple of 4",
                 (long long)a->out_stride_t);
@@ -127,6 +130,7 @@ smla::KParams make_params(const smla_args* a, int dev) {
   p.big_cache = (int64_t)a->num_pages * SMLA_PAGE * SMLA_ROW_BYTES > g_l2_bytes[dev] / 4 ? 1 : 0;
   p.err = g_err_ptr[dev];
   p.kv_format = a->kv_format;
+  p.nope = a->layout == SMLA_LAYOUT_NOPE ? 1 : 0;
   // one list: the second-list fields stay inert
   p.dual = 0;
   p.x_base = 0x7FFFFFFF;
@@ -268,7 +272,7 @@ int decode_launch(smla::KParams p, int width, int num_splits, void* workspace, s
 
 extern "C" {
 
-int32_t sparse_mla_abi_version(void) { return 3; }
+int32_t sparse_mla_abi_version(void) { return 4; }
 
 const char* sparse_mla_last_error(void) { return g_last_error; }
 

@@ -75,6 +75,8 @@ struct KParams {
   int64_t bt2_stride;
   int32_t bt2_cols;
   int32_t kv_format;  // 0: e4m3 codes, 1: int8 codes (both caches)
+  int32_t nope;       // 1: no rope (q is [T, H, 512]; row bytes [528, 656) are never read)
+  int32_t pad_;
   const int32_t* indices2;
   int64_t idx2_stride_t;
   const int32_t* topk_length2;  // nullptr: topk2

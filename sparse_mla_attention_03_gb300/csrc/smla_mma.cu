@@ -101,12 +101,12 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
     const int h = h0 + hh;
     uint8_t* qrow = smem + L::q + hh * QS;
     if (h < p.H) {
-      const __nv_bfloat16* qg = p.q + (int64_t)t * p.q_stride_t + (int64_t)h * kDQK;
+      const __nv_bfloat16* qg = p.q + (int64_t)t * p.q_stride_t + (int64_t)h * (p.nope ? kDNope : kDQK);
       float v[18];
       float amax = 0.f;
 #pragma unroll
       for (int i = 0; i < 18; ++i) {
-        v[i] = __bfloat162float(qg[i * 32 + lane]);
+        v[i] = (i < 16 || !p.nope) ? __bfloat162float(qg[i * 32 + lane]) : 0.f;  // no rope: zero q rope
         amax = fmaxf(amax, fabsf(v[i]));
       }
 #pragma unroll
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
         acc[n][3] = fmaf(scg8, tmp[n][3], acc[n][3]);
       }
     }
-    {  // rope dims: bf16 x bf16
+    if (!p.nope) {  // rope dims: bf16 x bf16 (without rope the row bytes there are padding)
       const uint4 ra0 = lds128(pg + swz(rg, 33 + tq) * 16);
       const uint4 ra1 = lds128(pg + swz(rg, 37 + tq) * 16);
       const uint4 rb0 = lds128(pg8 + swz(rg8, 33 + tq) * 16);

@@ -643,11 +643,17 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
               mma_lo(T_S, ag + (uint32_t)((kb2 * 16384 + st * 32) >> 4), bg + (uint32_t)((kb2 * 8192 + st * 32) >> 4),
                      id_f16, (g | kb2 | st) != 0);
         }
+        // the rope group is waited for even without rope (p.nope: its bytes are
+        // padding and its MMAs are skipped), so that the tile region where P^T
+        // will be written is no longer being stored to
         if (!mbar_wait_warp(bar(B_KV0 + 4), it & 1, s_abort, p.err)) return false;
         tc_fence_after();
+        if (!p.nope) {
 #pragma unroll
-        for (int st = 0; st < 4; ++st)
-          mma_lo(T_S, ad_rope + (uint32_t)((st * 32) >> 4), bd_q + (uint32_t)((8 * 8192 + st * 32) >> 4), id_bf16, 1);
+          for (int st = 0; st < 4; ++st)
+            mma_lo(T_S, ad_rope + (uint32_t)((st * 32) >> 4), bd_q + (uint32_t)((8 * 8192 + st * 32) >> 4), id_bf16,
+                   1);
+        }
         mma_commit(bar(B_SFULL));
         return true;
       };
@@ -698,8 +704,26 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     // in the q buffer by coalesced 16-byte cp.async, then converted in place;
     // thread c converts head c/2, chunks [36 (c%2), 36 (c%2) + 36) of its 72.
     {
-      const __nv_bfloat16* qsrc = p.q + (int64_t)t * p.q_stride_t + (int64_t)h0 * kDQK;
-      if ((reinterpret_cast<uintptr_t>(qsrc) & 15) == 0) {
+      const __nv_bfloat16* qsrc = p.q + (int64_t)t * p.q_stride_t + (int64_t)h0 * (p.nope ? kDNope : kDQK);
+      if (p.nope) {
+        // 512-dim heads (512 apart); the q buffer's rope chunks are zeroed
+        // (the rope MMAs are skipped without rope)
+        const unsigned short* qs = reinterpret_cast<const unsigned short*>(qsrc);
+#pragma unroll 2
+        for (int f = c; f < HG * 72; f += 128) {
+          const int hh = f / 72, ch = f % 72;
+          const uint32_t dst = sbase + q_chunk_off(hh, ch);
+          if (ch < 64) {
+            const unsigned short* e = qs + (int64_t)hh * kDNope + 8 * ch;
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = (uint32_t)__ldg(e + 2 * i) | ((uint32_t)__ldg(e + 2 * i + 1) << 16);
+            sts128(dst, make_uint4(w[0], w[1], w[2], w[3]));
+          } else {
+            sts128(dst, make_uint4(0u, 0u, 0u, 0u));
+          }
+        }
+      } else if ((reinterpret_cast<uintptr_t>(qsrc) & 15) == 0) {
 #pragma unroll 4
         for (int f = c; f < HG * 72; f += 128) cp_async16(sbase + q_chunk_off(f / 72, f % 72), qsrc + 8 * f, 16);
         cp_async_commit();

@@ -53,6 +53,7 @@ class Workload:
     extra_topk_length: Optional[torch.Tensor] = None  # int32 [T]
     extra_block_table: Optional[torch.Tensor] = None  # int32 [B, max_pages2]
     kv_format: str = "e4m3"  # code bytes of every cache: "e4m3" or "int8"
+    layout: str = "rope64"  # "rope64", or "nope": q is [T, H, 512] and row bytes [528:656) are padding
 
     @property
     def dual(self):
@@ -79,12 +80,16 @@ def pow2_scale_exponent(amax: np.ndarray) -> np.ndarray:
     return np.where(v > 0, e, 0)
 
 
-def make_cache(rng: np.random.Generator, num_pages: int, chunk_rows: int = 65536, kv_format: str = "e4m3") -> torch.Tensor:
+def make_cache(rng: np.random.Generator, num_pages: int, chunk_rows: int = 65536, kv_format: str = "e4m3",
+               scales: str = "pow2", layout: str = "rope64") -> torch.Tensor:
     """A paged cache ``[num_pages, 64, 656]`` of uint8 rows (see module docstring).
 
     ``kv_format="int8"``: the same row layout with signed int8 codes, per-128
     ``scale = amax / 127`` (fp32, not a power of two) and ``code =
-    rint(x / scale)`` clipped to [-127, 127]."""
+    rint(x / scale)`` clipped to [-127, 127].  ``scales="any"`` (e4m3 only):
+    ``scale = amax / 448`` as stored, not rounded to a power of two (GLM NSA
+    stores arbitrary fp32 scales).  ``layout="nope"``: bytes ``[528:656)``
+    are padding filled with 0xFF (a NaN pattern as bf16), never to be read."""
     n_rows = num_pages * PAGE
     out = np.empty((n_rows, ROW_BYTES), dtype=np.uint8)
     for lo in range(0, n_rows, chunk_rows):
@@ -96,6 +101,11 @@ def make_cache(rng: np.random.Generator, num_pages: int, chunk_rows: int = 65536
             scale = (np.maximum(amax, np.float32(1e-30)) / np.float32(127.0)).astype(np.float32)  # [n, 4]
             y = (x.reshape(n, 4, 128) / scale[:, :, None]).reshape(n, 512)
             codes = np.clip(np.rint(y), -127, 127).astype(np.int8).view(np.uint8)
+        elif scales == "any":
+            scale = (np.maximum(amax, np.float32(1e-30)) / np.float32(448.0)).astype(np.float32)
+            y = (x.reshape(n, 4, 128) / scale[:, :, None]).reshape(n, 512)
+            y = np.clip(y, -448.0, 448.0)
+            codes = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
         else:
             e = pow2_scale_exponent(amax)
             scale = np.ldexp(np.float32(1.0), e).astype(np.float32)  # [n, 4]
@@ -106,7 +116,7 @@ def make_cache(rng: np.random.Generator, num_pages: int, chunk_rows: int = 65536
         rope_bits = torch.from_numpy(rope).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint8)
         out[lo:hi, 0:512] = codes
         out[lo:hi, 512:528] = scale.astype("<f4").view(np.uint8).reshape(n, 16)
-        out[lo:hi, 528:656] = rope_bits.reshape(n, 128)
+        out[lo:hi, 528:656] = rope_bits.reshape(n, 128) if layout == "rope64" else 0xFF
     return torch.from_numpy(out.reshape(num_pages, PAGE, ROW_BYTES))
 
 
@@ -135,7 +145,7 @@ def _bf16(rng, shape):
 
 
 def make_prefill(name, T, H, ctx, topk, seed=0, sink="normal", ld=None, ragged=False,
-                 neg_prob=0.0, sm_scale=None, kv_format="e4m3") -> Workload:
+                 neg_prob=0.0, sm_scale=None, kv_format="e4m3", scales="pow2", layout="rope64") -> Workload:
     """Flat-addressed prefill: one context of ``ctx`` rows, ``topk`` unique ids per row.
 
     ``ragged``: topk_length ~ U{1..topk} per row and entries past it set to -1.
@@ -144,8 +154,9 @@ def make_prefill(name, T, H, ctx, topk, seed=0, sink="normal", ld=None, ragged=F
     """
     rng = np.random.default_rng(seed)
     assert ctx % PAGE == 0
-    kv = make_cache(rng, ctx // PAGE, kv_format=kv_format)
-    q = _bf16(rng, (T, H, D_QK))
+    kv = make_cache(rng, ctx // PAGE, kv_format=kv_format, scales=scales, layout=layout)
+    d_qk = D_QK if layout == "rope64" else D_V
+    q = _bf16(rng, (T, H, d_qk))
     ld = topk if ld is None else ld
     idx = np.full((T, ld), POISON, dtype=np.int64)
     idx[:, :topk] = unique_rows(rng, T, topk, ctx)
@@ -166,14 +177,14 @@ def make_prefill(name, T, H, ctx, topk, seed=0, sink="normal", ld=None, ragged=F
         s = None
     return Workload(
         name=name, q=q, kv=kv, indices=torch.from_numpy(idx.astype(np.int32)), topk=topk,
-        sm_scale=(1.0 / math.sqrt(D_QK)) if sm_scale is None else sm_scale,
-        topk_length=tl, attn_sink=s, kv_format=kv_format,
+        sm_scale=(1.0 / math.sqrt(d_qk)) if sm_scale is None else sm_scale,
+        topk_length=tl, attn_sink=s, kv_format=kv_format, layout=layout,
         meta=dict(T=T, H=H, ctx=ctx, topk=topk, ld=ld, seed=seed, ragged=ragged,
                   neg_prob=neg_prob, sink=sink, kv_format=kv_format))
 
 
 def make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=0, sink="normal",
-                kv_format="e4m3") -> Workload:
+                kv_format="e4m3", layout="rope64") -> Workload:
     """Paged decode: ``n_req`` requests, each its own context of ``ctx_per_req``
     logical positions mapped through a block table that is one shuffled
     permutation of all pages; ``topk`` unique logical ids per query token."""
@@ -181,9 +192,10 @@ def make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=0, sink=
     assert ctx_per_req % PAGE == 0
     pages_per_req = ctx_per_req // PAGE
     num_pages = n_req * pages_per_req
-    kv = make_cache(rng, num_pages, kv_format=kv_format)
+    kv = make_cache(rng, num_pages, kv_format=kv_format, layout=layout)
     T = n_req * tokens_per_req
-    q = _bf16(rng, (T, H, D_QK))
+    d_qk = D_QK if layout == "rope64" else D_V
+    q = _bf16(rng, (T, H, d_qk))
     bt = rng.permutation(num_pages).reshape(n_req, pages_per_req)
     idx = unique_rows(rng, T, topk, ctx_per_req)
     if sink == "normal":
@@ -194,9 +206,9 @@ def make_decode(name, n_req, tokens_per_req, H, ctx_per_req, topk, seed=0, sink=
         s = None
     return Workload(
         name=name, q=q, kv=kv, indices=torch.from_numpy(idx.astype(np.int32)), topk=topk,
-        sm_scale=1.0 / math.sqrt(D_QK), attn_sink=s,
+        sm_scale=1.0 / math.sqrt(d_qk), attn_sink=s,
         block_table=torch.from_numpy(bt.astype(np.int32)), tokens_per_req=tokens_per_req,
-        decode=True, kv_format=kv_format,
+        decode=True, kv_format=kv_format, layout=layout,
         meta=dict(n_req=n_req, tokens_per_req=tokens_per_req, H=H, ctx_per_req=ctx_per_req,
                   topk=topk, seed=seed, sink=sink))
 

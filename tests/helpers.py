@@ -29,7 +29,8 @@ def oracle_dual_for(wl, tokens=None):
         wl.extra_topk, wl.sm_scale, topk_length=np_(wl.topk_length), extra_topk_length=np_(wl.extra_topk_length),
         attn_sink=None if wl.attn_sink is None else wl.attn_sink.numpy().astype(np.float64),
         block_table=np_(wl.block_table), extra_block_table=np_(wl.extra_block_table),
-        tokens_per_req=wl.tokens_per_req, tokens=sel, q_selected=sel is not None, kv_format=wl.kv_format)
+        tokens_per_req=wl.tokens_per_req, tokens=sel, q_selected=sel is not None, kv_format=wl.kv_format,
+        layout=wl.layout)
 
 
 def oracle_for(wl, tokens=None, indices=None, topk=None, topk_length="wl", attn_sink="wl"):
@@ -43,7 +44,7 @@ def oracle_for(wl, tokens=None, indices=None, topk=None, topk_length="wl", attn_
                                 topk_length=None if tl is None else tl.numpy(),
                                 attn_sink=None if sk is None else sk.numpy().astype(np.float64),
                                 block_table=bt, tokens_per_req=wl.tokens_per_req, tokens=sel,
-                                q_selected=sel is not None, kv_format=wl.kv_format)
+                                q_selected=sel is not None, kv_format=wl.kv_format, layout=wl.layout)
 
 
 def assert_close(out_gpu, lse_gpu, out_ref, lse_ref, tag=""):

@@ -33,10 +33,34 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(binding.SYMBOLS), (set(names) ^ set(binding.SYMBOLS))
 
 
-def test_struct_layout_matches_header():
-    assert ctypes.sizeof(binding.SmlaArgs) == 144
-    assert binding.SmlaArgs.out.offset == 112
-    assert binding.SmlaArgs.sm_scale.offset == 96
+def _c_layout(struct, fields):
+    """sizeof and offsetof of a header struct, from a C program built with gcc."""
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    body = "".join(f'  printf("%zu\\n", offsetof({struct}, {f}));\n' for f in fields)
+    src = (f"#include <stddef.h>\n#include <stdio.h>\n#include \"sparse_mla.h\"\n"
+           f"int main(void) {{\n  printf(\"%zu\\n\", sizeof({struct}));\n{body}  return 0;\n}}\n")
+    with tempfile.TemporaryDirectory() as d:
+        c, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        with open(c, "w") as f:
+            f.write(src)
+        subprocess.run([cc, "-I", inc, c, "-o", exe], check=True)
+        vals = [int(x) for x in subprocess.run([exe], check=True, capture_output=True, text=True).stdout.split()]
+    return vals[0], dict(zip(fields, vals[1:]))
+
+
+@pytest.mark.parametrize("ctype,struct", [(binding.SmlaArgs, "smla_args"), (binding.SmlaExtraArgs, "smla_extra_args")])
+def test_struct_layout_matches_header(ctype, struct):
+    fields = [f for f, _ in ctype._fields_]
+    size, offs = _c_layout(struct, fields)
+    assert ctypes.sizeof(ctype) == size
+    for f in fields:
+        assert getattr(ctype, f).offset == offs[f], f
 
 
 def _args(**kw):
@@ -55,7 +79,7 @@ def _args(**kw):
 @pytest.mark.parametrize("bad", [
     dict(H=0), dict(H=129), dict(topk=0), dict(T=-1), dict(q_stride_t=100), dict(out_stride_t=8 * 512 + 2),
     dict(lse_stride_t=4), dict(idx_stride_t=10), dict(q=0), dict(kv=0x2001), dict(out=0x4002),
-    dict(kv_format=2), dict(sm_scale=float("nan")), dict(num_pages=-1),
+    dict(kv_format=2), dict(layout=2), dict(reserved1=1), dict(sm_scale=float("nan")), dict(num_pages=-1),
     dict(block_table=0x6000, bt_rows=1, bt_cols=8, bt_stride=8, tokens_per_req=2),  # 2 tokens/row x 1 row < 4
     dict(block_table=0x6000, bt_rows=4, bt_cols=8, bt_stride=4, tokens_per_req=1),  # stride < cols
 ])
@@ -90,4 +114,4 @@ def test_explicit_split_arithmetic(lib):
     assert lib.sparse_mla_decode_num_splits(4, 8, 640, 3) == 3
     ws = lib.sparse_mla_decode_workspace_size(128, 64, 2048, 8)
     assert ws == 128 * 64 * 8 * 512 * 4 + 128 * 64 * 8 * 4
-    assert lib.sparse_mla_abi_version() == 3
+    assert lib.sparse_mla_abi_version() == 4

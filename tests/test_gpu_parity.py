@@ -20,7 +20,7 @@ def run_prefill(wl, **kw):
     return binding.sparse_mla_prefill(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
                                       topk_length=d["topk_length"], attn_sink=d["attn_sink"],
                                       block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
-                                      kv_format=wl.kv_format, **kw)
+                                      kv_format=wl.kv_format, layout=wl.layout, **kw)
 
 
 def run_decode(wl, num_splits=0, **kw):
@@ -28,7 +28,7 @@ def run_decode(wl, num_splits=0, **kw):
     return binding.sparse_mla_decode(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
                                      topk_length=d["topk_length"], attn_sink=d["attn_sink"],
                                      block_table=d["block_table"], tokens_per_req=wl.tokens_per_req,
-                                     num_splits=num_splits, kv_format=wl.kv_format, **kw)
+                                     num_splits=num_splits, kv_format=wl.kv_format, layout=wl.layout, **kw)
 
 
 @pytest.fixture(autouse=True)
@@ -197,7 +197,8 @@ def run_dual(wl, decode=False, num_splits=0):
     d = to_dev(wl)
     kw = dict(topk=wl.topk, topk_length=d["topk_length"], extra_topk=wl.extra_topk,
               extra_topk_length=d["extra_topk_length"], attn_sink=d["attn_sink"], block_table=d["block_table"],
-              extra_block_table=d["extra_block_table"], tokens_per_req=wl.tokens_per_req, kv_format=wl.kv_format)
+              extra_block_table=d["extra_block_table"], tokens_per_req=wl.tokens_per_req, kv_format=wl.kv_format,
+              layout=wl.layout)
     if decode:
         return binding.sparse_mla_decode_dual(d["q"], d["kv"], d["indices"], d["extra_kv"], d["extra_indices"],
                                               wl.sm_scale, num_splits=num_splits, **kw)
@@ -325,6 +326,48 @@ def test_int8_differs_from_e4m3_reading():
     b, _ = run_prefill(wl)
     diff = (a.float() - b.float()).abs()  # codes 0x7F / 0xFF are NaN when read as e4m3
     assert torch.isnan(diff).any() or diff.max().item() > 1e-2
+
+
+# ----------------------------------------------------------------------------- other row layouts
+# GLM53_NOPE: no rope, q is [T, H, 512], row bytes [528, 656) are padding
+# (filled with 0xFF, a NaN pattern as bf16, by the generator: reading them
+# would poison the result)
+@pytest.mark.parametrize("H", [8, 16, 64, 128])
+def test_nope_prefill_ragged(H):
+    wl = inputs.make_prefill("nopep", T=6, H=H, ctx=2048, topk=300, seed=241 + H, ragged=True, layout="nope")
+    out, lse = run_prefill(wl)
+    assert_close(out, lse, *oracle_for(wl), tag=f"nope_prefill_H{H}")
+    assert binding.get_error_word() == 0
+
+
+@pytest.mark.parametrize("H,S", [(64, 0), (64, 3), (8, 2)])
+def test_nope_decode_paged(H, S):
+    wl = inputs.make_decode("noped", n_req=3, tokens_per_req=2, H=H, ctx_per_req=4096, topk=512, seed=251 + S,
+                            layout="nope", kv_format="int8" if S == 3 else "e4m3")
+    out, lse = run_decode(wl, num_splits=S)
+    assert_close(out, lse, *oracle_for(wl), tag=f"nope_decode_H{H}_S{S}")
+    assert binding.get_error_word() == 0
+
+
+def test_nope_dual_beyond_l2():
+    wl = inputs.make_dual_prefill("nopedual", T=4, H=64, ctx=65536, topk=256, extra_ctx=1024, extra_topk=128,
+                                  seed=261, ragged=True)
+    # rebuild both caches and q in the no-rope layout
+    nope = inputs.make_prefill("nopedual", T=4, H=64, ctx=65536, topk=256, seed=261, layout="nope")
+    wl.q, wl.kv, wl.layout, wl.sm_scale = nope.q, nope.kv, "nope", nope.sm_scale
+    wl.extra_kv = inputs.make_prefill("nopex", T=1, H=1, ctx=1024, topk=8, seed=262, layout="nope").kv
+    out, lse = run_dual(wl)
+    assert_close(out, lse, *oracle_dual_for(wl), tag="nope_dual")
+    assert binding.get_error_word() == 0
+
+
+# GLM_NSA: arbitrary (not power-of-two) fp32 scales on e4m3 codes
+@pytest.mark.parametrize("H", [8, 64])
+def test_arbitrary_scales(H):
+    wl = inputs.make_prefill("nsa", T=6, H=H, ctx=2048, topk=384, seed=271 + H, ragged=True, scales="any")
+    out, lse = run_prefill(wl)
+    assert_close(out, lse, *oracle_for(wl), tag=f"arbitrary_scales_H{H}")
+    assert binding.get_error_word() == 0
 
 
 # ----------------------------------------------------------------------------- full-size workloads

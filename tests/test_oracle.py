@@ -537,3 +537,60 @@ def test_int8_planted_mistakes_are_caught():
     # the row decoder reading int8 rows as e4m3 fails the row pin
     with pytest.raises(AssertionError):
         check_int8(decode_rows=lambda rows, fmt: O.decode_rows(rows, "e4m3"))
+
+
+# ----------------------------------------------------------------------------- no-rope layout (GLM53_NOPE)
+def check_nope(forward=O.sparse_mla_forward):
+    wl = inputs.make_prefill("nopepin", T=4, H=3, ctx=256, topk=90, seed=31, ragged=True, layout="nope")
+    sink = np.array([0.5, -0.4, 1.0])
+    out, lse = forward(q_f64(wl), wl.kv.numpy(), wl.indices.numpy(), wl.topk, wl.sm_scale,
+                       topk_length=wl.topk_length.numpy(), attn_sink=sink, layout="nope")
+    # the 0xFF padding (NaN as bf16) is never read
+    assert np.isfinite(out).all() and not np.isnan(lse).any()
+    # equals the rope layout with a zero q rope and zero rope bytes
+    kv = wl.kv.numpy().copy()
+    kv[..., 528:656] = 0
+    q576 = np.concatenate([q_f64(wl), np.zeros((wl.T, wl.H, 64))], axis=2)
+    out_r, lse_r = O.sparse_mla_forward(q576, kv, wl.indices.numpy(), wl.topk, wl.sm_scale,
+                                        topk_length=wl.topk_length.numpy(), attn_sink=sink)
+    np.testing.assert_allclose(out, out_r, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_r, rtol=1e-12, atol=1e-12)
+    # dense coverage against SDPA over 512-dim keys
+    rng = np.random.default_rng(4)
+    dn = inputs.make_prefill("nopedense", T=2, H=3, ctx=128, topk=128, seed=41, sink=None, layout="nope")
+    dn.indices = torch.from_numpy(np.stack([rng.permutation(128) for _ in range(2)]).astype(np.int32))
+    od, ld = forward(q_f64(dn), dn.kv.numpy(), dn.indices.numpy(), 128, dn.sm_scale, attn_sink=sink,
+                     layout="nope")
+    K = dequant_via_torch(dn.kv.numpy().reshape(-1, 656)).numpy()[:, :512]
+    for t in range(dn.T):
+        qt = torch.from_numpy(q_f64(dn)[t]).reshape(1, 3, 1, 512)
+        Kt = torch.as_tensor(K).reshape(1, 1, -1, 512).expand(1, 3, -1, 512)
+        Kt = torch.cat([Kt, torch.zeros(1, 3, 1, 512, dtype=torch.float64)], dim=2)
+        mask = torch.zeros(1, 3, 1, Kt.shape[2], dtype=torch.float64)
+        mask[0, :, 0, -1] = torch.as_tensor(sink)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, Kt, Kt, attn_mask=mask, scale=dn.sm_scale)
+        np.testing.assert_allclose(od[t], ref.reshape(3, 512).numpy(), rtol=0, atol=1e-12)
+        sc = (qt.reshape(3, 512) @ torch.as_tensor(K).T) * dn.sm_scale
+        np.testing.assert_allclose(ld[t], torch.logsumexp(sc, dim=1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_nope_layout_pins():
+    check_nope()
+
+
+def test_nope_planted_mistake_reads_padding():
+    orig = O.decode_rows
+
+    def reads_padding(rows, kv_format="e4m3", layout="rope64"):
+        k = orig(rows, kv_format, "rope64")
+        return k[:, :512] + 0.0 * k[:, 512:].sum(axis=1, keepdims=True) if layout == "nope" else k
+
+    def forward(*a, **kw):
+        O.decode_rows = reads_padding
+        try:
+            return O.sparse_mla_forward(*a, **kw)
+        finally:
+            O.decode_rows = orig
+
+    with pytest.raises(AssertionError):
+        check_nope(forward)
