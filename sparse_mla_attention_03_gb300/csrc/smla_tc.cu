@@ -554,6 +554,118 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
   }
 }
 
+// q of one token, loaded and converted while the producers gather the first
+// tile, by the 256 threads of the softmax warps and the last warpgroup (whose
+// MMA-issue warp waits for q anyway; the other three have no other work).  The
+// 64 head rows (one contiguous 72 KB block, or 64 KB without rope) are copied
+// into their swizzled places in the q buffer, then converted in place: thread
+// qc handles head qc/4, chunks [18 (qc%4), 18 (qc%4) + 18) of its 72.  Each
+// head gets a power-of-two prescale putting its largest |q| in [2^14, 2^15);
+// the exponent of that maximum is the largest exponent field of the head's
+// bf16 values (an integer max over 16-bit halves), except when it is 0 or 255
+// (all zero or subnormal; Inf/NaN), where the float maximum decides.
+__device__ __forceinline__ void load_q(const KParams& p, uint8_t* smem, uint32_t sbase, int t, int h0, int qc,
+                                       float* s_qmul, float* s_mref, float* s_mneg, uint32_t bars) {
+  const __nv_bfloat16* qsrc = p.q + (int64_t)t * p.q_stride_t + (int64_t)h0 * (p.nope ? kDNope : kDQK);
+  if (p.nope) {
+    // 512-dim heads (512 apart); the q buffer's rope chunks are zeroed (the
+    // rope MMAs are skipped without rope)
+    const unsigned short* qs = reinterpret_cast<const unsigned short*>(qsrc);
+#pragma unroll 2
+    for (int f = qc; f < HG * 72; f += 256) {
+      const int hh = f / 72, ch = f % 72;
+      const uint32_t dst = sbase + q_chunk_off(hh, ch);
+      if (ch < 64) {
+        const unsigned short* e = qs + (int64_t)hh * kDNope + 8 * ch;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = (uint32_t)__ldg(e + 2 * i) | ((uint32_t)__ldg(e + 2 * i + 1) << 16);
+        sts128(dst, make_uint4(w[0], w[1], w[2], w[3]));
+      } else {
+        sts128(dst, make_uint4(0u, 0u, 0u, 0u));
+      }
+    }
+  } else if ((reinterpret_cast<uintptr_t>(qsrc) & 15) == 0) {
+#pragma unroll 2
+    for (int f = qc; f < HG * 72; f += 256) cp_async16(sbase + q_chunk_off(f / 72, f % 72), qsrc + 8 * f, 16);
+    cp_async_commit();
+    cp_async_wait<0>();
+  } else {
+    const unsigned short* qs = reinterpret_cast<const unsigned short*>(qsrc);
+#pragma unroll 2
+    for (int f = qc; f < HG * 72; f += 256) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = (uint32_t)__ldg(qs + 8 * f + 2 * i) | ((uint32_t)__ldg(qs + 8 * f + 2 * i + 1) << 16);
+      sts128(sbase + q_chunk_off(f / 72, f % 72), make_uint4(w[0], w[1], w[2], w[3]));
+    }
+  }
+  named_bar(2, 256);
+  const int hh = qc >> 2, quarter = qc & 3;
+  uint32_t m = 0;
+#pragma unroll 3
+  for (int k = 0; k < 18; ++k) {
+    const uint4 v = *reinterpret_cast<const uint4*>(smem + q_chunk_off(hh, 18 * quarter + k));
+    m = __vmaxu2(m, v.x & 0x7F807F80u);
+    m = __vmaxu2(m, v.y & 0x7F807F80u);
+    m = __vmaxu2(m, v.z & 0x7F807F80u);
+    m = __vmaxu2(m, v.w & 0x7F807F80u);
+  }
+  m = max(m & 0xFFFFu, m >> 16);
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  const int ef = (int)(m >> 7);  // largest exponent field of the head
+  int e = ef - 141;              // the exponent of max|q| is ef - 126; prescale to [2^14, 2^15)
+  e = e < -100 ? -100 : (e > 100 ? 100 : e);
+  if (__any_sync(0xffffffffu, ef == 0 || ef == 255)) {
+    float amax = 0.f;
+#pragma unroll 2
+    for (int k = 0; k < 18; ++k) {
+      const uint4 v = *reinterpret_cast<const uint4*>(smem + q_chunk_off(hh, 18 * quarter + k));
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] & 0xFFFF0000u)));
+      }
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if (ef == 0 || ef == 255) e = q_prescale_exp(amax);
+  }
+  const float down = pow2f(-e);
+#pragma unroll 3
+  for (int k = 0; k < 18; ++k) {
+    const int ch = 18 * quarter + k;  // 8 dims: 8ch .. 8ch+7
+    const uint32_t off = q_chunk_off(hh, ch);
+    const uint4 v = *reinterpret_cast<const uint4*>(smem + off);
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = __uint_as_float(wv[i] << 16) * down;
+      const float b = __uint_as_float(wv[i] & 0xFFFF0000u) * down;
+      if (ch < 64) {
+        const __half2 hv = __floats2half2_rn(a, b);
+        o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+      } else {
+        const __nv_bfloat162 bv = __floats2bfloat162_rn(a, b);
+        o[i] = *reinterpret_cast<const uint32_t*>(&bv);
+      }
+    }
+    sts128(sbase + off, make_uint4(o[0], o[1], o[2], o[3]));
+  }
+  if (quarter == 0) {
+    s_qmul[hh] = p.sm_scale * kLog2e * pow2f(e);
+    s_mref[hh] = -INFINITY;
+    s_mneg[hh] = 0.f;
+  }
+  fence_proxy_async();
+  mbar_arrive(bars + 8u * B_QCONV);  // q is ready for the S^T MMAs
+  named_bar(2, 256);                 // q, s_qmul and s_mref visible to the softmax warps and the issuer
+}
+
 template <bool kEarly, bool kDual, bool kInt8>
 __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -595,7 +707,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       mbar_init(bar(B_PFULL), 128);
       for (int c = 0; c < 4; ++c) mbar_init(bar(B_PV0 + c), 1);
       mbar_init(bar(B_DRAIN), 1);
-      mbar_init(bar(B_QCONV), 128);
+      mbar_init(bar(B_QCONV), 256);
       *s_abort = 0;
       *s_flag = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -619,6 +731,8 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   } else if (warp >= W_MMA) {
     // ============================================================ MMA issue (warp 12; 13-15 idle)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    load_q(p, smem, sbase, t, h0, tid - 256, reinterpret_cast<float*>(smem + OFF_QMUL),
+           reinterpret_cast<float*>(smem + OFF_MREF), reinterpret_cast<float*>(smem + OFF_MNEG), bars);
     if (warp == W_MMA) {
       const uint32_t id_f16 = idesc(0, 0, 0);
       const uint32_t id_bf16 = idesc(1, 0, 0);
@@ -699,92 +813,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     // read now so that the load is long done by the epilogue
     const float sink_lo = (q4 == 0 && p.attn_sink) ? __ldg(p.attn_sink + h0 + lane) : 0.f;
     const float sink_hi = (q4 == 0 && p.attn_sink) ? __ldg(p.attn_sink + h0 + lane + 32) : 0.f;
-    // q of this token, while the producers gather the first tile: the 64 head
-    // rows (one contiguous 72 KB block) are copied into their swizzled places
-    // in the q buffer by coalesced 16-byte cp.async, then converted in place;
-    // thread c converts head c/2, chunks [36 (c%2), 36 (c%2) + 36) of its 72.
-    {
-      const __nv_bfloat16* qsrc = p.q + (int64_t)t * p.q_stride_t + (int64_t)h0 * (p.nope ? kDNope : kDQK);
-      if (p.nope) {
-        // 512-dim heads (512 apart); the q buffer's rope chunks are zeroed
-        // (the rope MMAs are skipped without rope)
-        const unsigned short* qs = reinterpret_cast<const unsigned short*>(qsrc);
-#pragma unroll 2
-        for (int f = c; f < HG * 72; f += 128) {
-          const int hh = f / 72, ch = f % 72;
-          const uint32_t dst = sbase + q_chunk_off(hh, ch);
-          if (ch < 64) {
-            const unsigned short* e = qs + (int64_t)hh * kDNope + 8 * ch;
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) w[i] = (uint32_t)__ldg(e + 2 * i) | ((uint32_t)__ldg(e + 2 * i + 1) << 16);
-            sts128(dst, make_uint4(w[0], w[1], w[2], w[3]));
-          } else {
-            sts128(dst, make_uint4(0u, 0u, 0u, 0u));
-          }
-        }
-      } else if ((reinterpret_cast<uintptr_t>(qsrc) & 15) == 0) {
-#pragma unroll 4
-        for (int f = c; f < HG * 72; f += 128) cp_async16(sbase + q_chunk_off(f / 72, f % 72), qsrc + 8 * f, 16);
-        cp_async_commit();
-        cp_async_wait<0>();
-      } else {
-        const unsigned short* qs = reinterpret_cast<const unsigned short*>(qsrc);
-#pragma unroll 2
-        for (int f = c; f < HG * 72; f += 128) {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            w[i] = (uint32_t)__ldg(qs + 8 * f + 2 * i) | ((uint32_t)__ldg(qs + 8 * f + 2 * i + 1) << 16);
-          sts128(sbase + q_chunk_off(f / 72, f % 72), make_uint4(w[0], w[1], w[2], w[3]));
-        }
-      }
-      named_bar(1, 128);
-      const int hh = c >> 1, half = c & 1;
-      float amax = 0.f;
-#pragma unroll 4
-      for (int k = 0; k < 36; ++k) {
-        const uint4 v = *reinterpret_cast<const uint4*>(smem + q_chunk_off(hh, 36 * half + k));
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] << 16)));
-          amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] & 0xFFFF0000u)));
-        }
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      const int e = q_prescale_exp(amax);
-      const float down = pow2f(-e);
-#pragma unroll 4
-      for (int k = 0; k < 36; ++k) {
-        const int ch = 36 * half + k;  // 8 dims: 8ch .. 8ch+7
-        const uint32_t off = q_chunk_off(hh, ch);
-        const uint4 v = *reinterpret_cast<const uint4*>(smem + off);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float a = __uint_as_float(wv[i] << 16) * down;
-          const float b = __uint_as_float(wv[i] & 0xFFFF0000u) * down;
-          if (ch < 64) {
-            const __half2 hv = __floats2half2_rn(a, b);
-            o[i] = *reinterpret_cast<const uint32_t*>(&hv);
-          } else {
-            const __nv_bfloat162 bv = __floats2bfloat162_rn(a, b);
-            o[i] = *reinterpret_cast<const uint32_t*>(&bv);
-          }
-        }
-        sts128(sbase + off, make_uint4(o[0], o[1], o[2], o[3]));
-      }
-      if (half == 0) {
-        s_qmul[hh] = p.sm_scale * kLog2e * pow2f(e);
-        s_mref[hh] = -INFINITY;
-        s_mneg[hh] = 0.f;
-      }
-    }
-    fence_proxy_async();
-    mbar_arrive(bar(B_QCONV));  // q is ready for the S^T MMAs
-    named_bar(1, 128);  // q, s_qmul and s_mref visible to all softmax warps and the issuer
+    load_q(p, smem, sbase, t, h0, c, s_qmul, s_mref, s_mneg, bars);
 
     // running sums of P per head: lane l keeps heads l and l+32 of this warp's
     // 32 candidates (summed over the warp by a transpose-reduction per tile)

@@ -192,6 +192,22 @@ def test_cache_beyond_l2_paged_decode(S):
     assert binding.get_error_word() == 0
 
 
+@pytest.mark.parametrize("H", [8, 64])
+def test_q_heads_zero_subnormal_and_large(H):
+    # the per-head q prescale: an all-zero head, a head of bf16 subnormals (the
+    # exponent-field shortcut falls back to the float maximum) and large heads
+    wl = inputs.make_prefill("qext", T=3, H=H, ctx=1024, topk=200, seed=281)
+    q = wl.q.clone()
+    q[:, 0] = 0
+    q[:, 1] = (q[:, 1].float() * 1e-39).to(torch.bfloat16)
+    q[:, 2] = (q[:, 2].float() * 30.0).to(torch.bfloat16)
+    q[:, H - 1] = (q[:, H - 1].float() * 1e-3).to(torch.bfloat16)
+    wl.q = q
+    out, lse = run_prefill(wl)
+    assert_close(out, lse, *oracle_for(wl), tag=f"q_extreme_H{H}")
+    assert binding.get_error_word() == 0
+
+
 # ----------------------------------------------------------------------------- dual-cache form
 def run_dual(wl, decode=False, num_splits=0):
     d = to_dev(wl)
