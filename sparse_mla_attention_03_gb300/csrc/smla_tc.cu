@@ -45,7 +45,7 @@ namespace tc_path {
 
 constexpr int BM = 128;  // candidate rows per tile (MMA M)
 constexpr int HG = 64;   // heads per CTA (MMA N)
-constexpr int NT = 512;   // 8 producer warps, 4 softmax warps, 1 MMA warp, 3 idle
+constexpr int NT = 512;   // 8 producer warps, 4 softmax warps, 1 MMA warp, 3 helpers (q, epilogue)
 constexpr int W_SOFT = 8;
 constexpr int W_MMA = 12;
 constexpr uint64_t kTimeoutNs = 1000000000ull;
@@ -554,6 +554,95 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
   }
 }
 
+// Epilogue: parts [part_lo, part_hi) of the 8 (d_v chunk, 32-head half)
+// parts of O^T, by a warp whose TMEM lane quarter is q4.  s_alpha holds
+// the per-head normaliser.
+__device__ __forceinline__ void store_parts(const KParams& p, const float* s_alpha, uint32_t T_O,
+                                            uint32_t lane_off, int t, int h0, int split, int ntiles, int q4,
+                                            int lane, int part_lo, int part_hi) {
+  const bool final_out = p.ws_o == nullptr;
+  // O^T -> registers, 32 head columns at a time -> two transpose stages
+  // through lane pairs and quads: lane l ends up with 4 consecutive d_v
+  // values (4*(l/4) .. +3 of this warp's 32) for 8 heads
+  // (hq = 32*half + 16*(l&1) + 8*((l>>1)&1) + j), stored as one 8-byte
+  // (bf16 out) or 16-byte (fp32 partial) word per head.
+  const bool odd = lane & 1, hi2 = lane & 2;
+  const bool out_al8 = ((reinterpret_cast<uintptr_t>(p.out) | (uintptr_t)(p.out_stride_t * 2)) & 7) == 0;
+#pragma unroll 1
+  for (int part = part_lo; part < part_hi; ++part) {
+    const int ch = part >> 1, half = part & 1;
+    const int dv0 = 128 * ch + 32 * q4 + 4 * (lane >> 2);
+    const int hq = 32 * half + 16 * (lane & 1) + 8 * ((lane >> 1) & 1);
+    float o[32];
+    if (ntiles > 0) {
+      tmem_ld16(T_O + 64 * ch + 32 * half + lane_off, o);
+      tmem_ld16(T_O + 64 * ch + 32 * half + 16 + lane_off, o + 16);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int h = 0; h < 32; ++h) o[h] = 0.f;
+    }
+#pragma unroll
+    for (int h4 = 0; h4 < 8; ++h4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(s_alpha + 32 * half + 4 * h4);
+      o[4 * h4 + 0] *= a4.x;
+      o[4 * h4 + 1] *= a4.y;
+      o[4 * h4 + 2] *= a4.z;
+      o[4 * h4 + 3] *= a4.w;
+    }
+    if (final_out) {
+      uint32_t wv[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float send = odd ? o[j] : o[16 + j];
+        const float keep = odd ? o[16 + j] : o[j];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+        const __nv_bfloat162 bv = odd ? __floats2bfloat162_rn(recv, keep) : __floats2bfloat162_rn(keep, recv);
+        wv[j] = *reinterpret_cast<const uint32_t*>(&bv);
+      }
+      __nv_bfloat16* ob = p.out + (int64_t)t * p.out_stride_t + (int64_t)(h0 + hq) * kDV + dv0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t send = hi2 ? wv[j] : wv[8 + j];
+        const uint32_t keep = hi2 ? wv[8 + j] : wv[j];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+        const uint2 st = hi2 ? make_uint2(recv, keep) : make_uint2(keep, recv);
+        if (out_al8) {
+          *reinterpret_cast<uint2*>(ob + (int64_t)j * kDV) = st;
+        } else {
+          unsigned short* os = reinterpret_cast<unsigned short*>(ob + (int64_t)j * kDV);
+          os[0] = (unsigned short)(st.x & 0xFFFFu);
+          os[1] = (unsigned short)(st.x >> 16);
+          os[2] = (unsigned short)(st.y & 0xFFFFu);
+          os[3] = (unsigned short)(st.y >> 16);
+        }
+      }
+    } else {
+      float2 f2[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float send = odd ? o[j] : o[16 + j];
+        const float keep = odd ? o[16 + j] : o[j];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+        f2[j] = odd ? make_float2(recv, keep) : make_float2(keep, recv);
+      }
+      const int64_t hstride = (int64_t)p.num_splits * kDV;
+      float* wb = p.ws_o + (((int64_t)t * p.H + h0 + hq) * p.num_splits + split) * kDV + dv0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 send = hi2 ? f2[j] : f2[8 + j];
+        const float2 keep = hi2 ? f2[8 + j] : f2[j];
+        float2 recv;
+        recv.x = __shfl_xor_sync(0xffffffffu, send.x, 2);
+        recv.y = __shfl_xor_sync(0xffffffffu, send.y, 2);
+        const float4 st = hi2 ? make_float4(recv.x, recv.y, keep.x, keep.y)
+                              : make_float4(keep.x, keep.y, recv.x, recv.y);
+        *reinterpret_cast<float4*>(wb + (int64_t)j * hstride) = st;
+      }
+    }
+  }
+}
+
 // q of one token, loaded and converted while the producers gather the first
 // tile, by the 256 threads of the softmax warps and the last warpgroup (whose
 // MMA-issue warp waits for q anyway; the other three have no other work).  The
@@ -696,6 +785,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_FLAGS);
   volatile int* s_flag = reinterpret_cast<volatile int*>(smem + OFF_FLAGS + 4);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_FLAGS + 8);
+  volatile int* s_epi = reinterpret_cast<volatile int*>(smem + OFF_FLAGS + 12);  // epilogue runs
   const uint32_t bars = sbase + OFF_MISC;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
@@ -729,8 +819,8 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 136;" ::: "memory");
     producer<kEarly, kDual, kInt8>(p, smem, sbase, bars, t, ts.len1, lo, hi, ntiles, warp, lane, s_abort);
   } else if (warp >= W_MMA) {
-    // ============================================================ MMA issue (warp 12; 13-15 idle)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    // ============================================ q conversion, MMA issue (warp 12), epilogue
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
     load_q(p, smem, sbase, t, h0, tid - 256, reinterpret_cast<float*>(smem + OFF_QMUL),
            reinterpret_cast<float*>(smem + OFF_MREF), reinterpret_cast<float*>(smem + OFF_MNEG), bars);
     if (warp == W_MMA) {
@@ -803,9 +893,16 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       }
       __syncwarp();
     }
+    // second half of the epilogue (every issued MMA has completed: the issuer
+    // drained them, and the softmax warps waited for the last PV)
+    named_bar(2, 256);
+    if (*s_epi) {
+      tc_fence_after();
+      store_parts(p, s_alpha, T_O, (uint32_t)((warp & 3) * 32) << 16, t, h0, split, ntiles, warp & 3, lane, 4, 8);
+    }
   } else {
     // ============================================================ softmax + epilogue
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 160;" ::: "memory");
     const int q4 = warp & 3;
     const int c = q4 * 32 + lane;  // TMEM lane: candidate (S^T) / dv row (O^T)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -971,87 +1068,12 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
         }
       }
       named_bar(1, 128);
-      // O^T -> registers, 32 head columns at a time -> two transpose stages
-      // through lane pairs and quads: lane l ends up with 4 consecutive d_v
-      // values (4*(l/4) .. +3 of this warp's 32) for 8 heads
-      // (hq = 32*half + 16*(l&1) + 8*((l>>1)&1) + j), stored as one 8-byte
-      // (bf16 out) or 16-byte (fp32 partial) word per head.
-      const bool odd = lane & 1, hi2 = lane & 2;
-      const bool out_al8 = ((reinterpret_cast<uintptr_t>(p.out) | (uintptr_t)(p.out_stride_t * 2)) & 7) == 0;
-#pragma unroll 1
-      for (int part = 0; part < 8; ++part) {
-        const int ch = part >> 1, half = part & 1;
-        const int dv0 = 128 * ch + 32 * q4 + 4 * (lane >> 2);
-        const int hq = 32 * half + 16 * (lane & 1) + 8 * ((lane >> 1) & 1);
-        float o[32];
-        if (ntiles > 0) {
-          tmem_ld16(T_O + 64 * ch + 32 * half + lane_off, o);
-          tmem_ld16(T_O + 64 * ch + 32 * half + 16 + lane_off, o + 16);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int h = 0; h < 32; ++h) o[h] = 0.f;
-        }
-#pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-          const float4 a4 = *reinterpret_cast<const float4*>(s_alpha + 32 * half + 4 * h4);
-          o[4 * h4 + 0] *= a4.x;
-          o[4 * h4 + 1] *= a4.y;
-          o[4 * h4 + 2] *= a4.z;
-          o[4 * h4 + 3] *= a4.w;
-        }
-        if (final_out) {
-          uint32_t wv[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float send = odd ? o[j] : o[16 + j];
-            const float keep = odd ? o[16 + j] : o[j];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            const __nv_bfloat162 bv = odd ? __floats2bfloat162_rn(recv, keep) : __floats2bfloat162_rn(keep, recv);
-            wv[j] = *reinterpret_cast<const uint32_t*>(&bv);
-          }
-          __nv_bfloat16* ob = p.out + (int64_t)t * p.out_stride_t + (int64_t)(h0 + hq) * kDV + dv0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t send = hi2 ? wv[j] : wv[8 + j];
-            const uint32_t keep = hi2 ? wv[8 + j] : wv[j];
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
-            const uint2 st = hi2 ? make_uint2(recv, keep) : make_uint2(keep, recv);
-            if (out_al8) {
-              *reinterpret_cast<uint2*>(ob + (int64_t)j * kDV) = st;
-            } else {
-              unsigned short* os = reinterpret_cast<unsigned short*>(ob + (int64_t)j * kDV);
-              os[0] = (unsigned short)(st.x & 0xFFFFu);
-              os[1] = (unsigned short)(st.x >> 16);
-              os[2] = (unsigned short)(st.y & 0xFFFFu);
-              os[3] = (unsigned short)(st.y >> 16);
-            }
-          }
-        } else {
-          float2 f2[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float send = odd ? o[j] : o[16 + j];
-            const float keep = odd ? o[16 + j] : o[j];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            f2[j] = odd ? make_float2(recv, keep) : make_float2(keep, recv);
-          }
-          const int64_t hstride = (int64_t)p.num_splits * kDV;
-          float* wb = p.ws_o + (((int64_t)t * p.H + h0 + hq) * p.num_splits + split) * kDV + dv0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float2 send = hi2 ? f2[j] : f2[8 + j];
-            const float2 keep = hi2 ? f2[8 + j] : f2[j];
-            float2 recv;
-            recv.x = __shfl_xor_sync(0xffffffffu, send.x, 2);
-            recv.y = __shfl_xor_sync(0xffffffffu, send.y, 2);
-            const float4 st = hi2 ? make_float4(recv.x, recv.y, keep.x, keep.y)
-                                  : make_float4(keep.x, keep.y, recv.x, recv.y);
-            *reinterpret_cast<float4*>(wb + (int64_t)j * hstride) = st;
-          }
-        }
-      }
     }
+    // the last warpgroup stores half of the parts: s_alpha and the outcome
+    // are published to it by the barrier below
+    if (warp == W_SOFT && lane == 0) *s_epi = alive ? 1 : 0;
+    named_bar(2, 256);
+    if (alive) store_parts(p, s_alpha, T_O, lane_off, t, h0, split, ntiles, q4, lane, 0, 4);
   }
   tc_fence_before();
   __syncthreads();
