@@ -193,8 +193,8 @@ smla::KParams make_params_dual(const smla_args* a, const smla_extra_args* x, int
 }
 
 // Decode split choice.  An explicit request is honoured up to the number of
-// 64-slot chunks; the automatic choice keeps splitting while the grid is below
-// two waves and every split still holds at least 4 chunks.
+// 64-slot chunks; the automatic choice minimises waves x CTA length for the
+// kernel that will run (measured against split sweeps on GB300).
 int splits_for(int T, int H, int topk, int num_splits, int num_sms) {
   const int chunks = (topk + 63) / 64;
   int S;
@@ -220,11 +220,25 @@ int splits_for(int T, int H, int topk, int num_splits, int num_sms) {
       }
     }
   } else {
+    // warp-MMA kernel: the same waves x CTA-length model, with a wave of
+    // SMs x resident CTAs (4 per SM for 8-head CTAs, 2 for 16-head CTAs), a
+    // fixed cost of about 1.5 64-slot chunks, one unit per chunk, and 0.05
+    // units per split for the combine's merge
     const int hpc = smla::heads_per_cta(H);
+    const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 148) * (hpc == 8 ? 4 : 2);
     const int64_t base = (int64_t)T * ((H + hpc - 1) / hpc);
-    const int64_t target = 2LL * (num_sms > 0 ? num_sms : 148);
+    double best = 0.0;
     S = 1;
-    while (base * (S * 2) <= target && chunks / (S * 2) >= 4 && S * 2 <= SMLA_MAX_SPLITS) S *= 2;
+    for (int s = 1; s <= SMLA_MAX_SPLITS && s <= chunks; ++s) {
+      const int per = (chunks + s - 1) / s;
+      if (s > 1 && (chunks + per - 1) / per < s) continue;
+      const double waves = (double)((base * s + cap - 1) / cap);
+      const double cost = waves * (1.5 + per) + 0.05 * s;
+      if (s == 1 || cost < best * 0.97) {
+        best = cost;
+        S = s;
+      }
+    }
   }
   if (S < 1) S = 1;
   // effective count: chunks per split rounded up, then splits that hold slots
