@@ -107,11 +107,20 @@ def dram_traffic(workload):
         return None, None
     h = hashlib.sha256()
     for src in rec["sources"]:
-        with open(os.path.join(ROOT, src), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, src)) as f:
+            h.update(_code_only(f.read()).encode())
     if h.hexdigest() != rec["sources_sha256"]:
         return None, "kernel changed since the capture"
     return rec["dram_bytes_per_launch"], rec["capture"]
+
+
+def _code_only(src):
+    """C++ source without comments, trailing blanks and empty lines: the text
+    the kernel's code depends on (comment edits keep a capture valid)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.split("\n") if line.strip())
 
 
 def load_peaks():

@@ -20,19 +20,24 @@
 //          reused for P^T [128 cand x 64 h] f16 once S^T is done.
 //   q       72 KB: q of the token, nope f16 / rope bf16, B operand of S^T.
 //
-// Warp roles (384 threads, so that each thread may hold 168 registers):
+// Warp roles (512 threads; setmaxnreg gives 136 / 160 / 80 registers):
 //   warps 0-7   producers: warp w gathers rows 16w..16w+15 of each tile with
-//               coalesced 16-byte loads, converts e4m3 -> f16 times the row's
-//               scale (exact while |value| <= 65504) and stores it swizzled; the
-//               bf16 rope is copied as is.  The loads of tile i+1 are issued as
-//               soon as tile i is stored.
+//               coalesced 16-byte loads, converts the codes (e4m3 or int8) to
+//               f16 times the row's scale and stores them swizzled; the bf16
+//               rope is copied as is.  The next tile's rows are loaded in one
+//               burst after a tile is stored (L2-resident cache) or group by
+//               group as soon as each group is stored, with an L2 prefetch
+//               one tile further ahead (kEarly: cache beyond L2).
 //   warps 8-11  softmax/epilogue: thread = TMEM lane.  Per tile it reads its
 //               candidate's 64 scores once, keeps a per-head reference max that
 //               is only raised when a score exceeds it by 2^8 (then O^T columns
 //               and the sums are rescaled), writes P (f16) for the PV MMA and
 //               adds P into per-head sums with warp transpose-reductions.
-//               Lane 0 of warp 8 also allocates TMEM and issues every MMA:
-//               S^T of a tile before that tile's softmax, PV after it.
+//   warp 12     MMA issue: S^T of a tile group by group as the producers
+//               release them, PV after the softmax; one converged warp issuing
+//               through elect.sync.
+//   warps 12-15 with warps 8-11: the load and conversion of q before the first
+//               tile, and half of the epilogue's stores after the last.
 //
 // Every mbarrier wait is bounded (about one second of global time); on timeout
 // the CTA sets the error word, stops, drains its issued MMAs, frees TMEM and
