@@ -100,6 +100,23 @@ def test_noncontiguous_views_written_in_place():
     assert torch.all(obuf[:, 8:] == 7.0) and torch.all(lbuf[:, 8:] == 7.0)
 
 
+@pytest.mark.parametrize("pad", [4, 8])
+def test_tc_out_rows_with_padding(pad):
+    # out rows padded by 4 or 8 elements (rows 8- or 16-byte aligned) of a
+    # wider buffer, written in place; the padding is left untouched
+    wl = inputs.make_prefill("outpad", T=5, H=64, ctx=2048, topk=320, seed=291 + pad, ragged=True)
+    d = to_dev(wl)
+    row = 64 * 512 + pad
+    flat = torch.full((5 * row,), 3.0, dtype=torch.bfloat16, device="cuda")
+    out = flat.as_strided((5, 64, 512), (row, 512, 1))
+    o, lse = binding.sparse_mla_prefill(d["q"], d["kv"], d["indices"], wl.sm_scale, topk=wl.topk,
+                                        topk_length=d["topk_length"], attn_sink=d["attn_sink"], out=out)
+    assert o.data_ptr() == flat.data_ptr()
+    assert_close(out, lse, *oracle_for(wl), tag=f"outpad{pad}")
+    pads = flat.view(5, row)[:, 64 * 512:]
+    assert torch.all(pads == 3.0)
+
+
 def test_single_valid_index_and_empty_rows():
     wl = inputs.make_prefill("single", T=4, H=16, ctx=1024, topk=128, seed=51)
     idx = torch.full((4, 128), -1, dtype=torch.int32)
