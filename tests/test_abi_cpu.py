@@ -115,3 +115,36 @@ def test_explicit_split_arithmetic(lib):
     ws = lib.sparse_mla_decode_workspace_size(128, 64, 2048, 8)
     assert ws == 128 * 64 * 8 * 512 * 4 + 128 * 64 * 8 * 4
     assert lib.sparse_mla_abi_version() == 4
+
+
+# ----------------------------------------------------------------------------- bench helpers (host logic)
+def test_bench_traffic_record_tracks_kernel_sources(tmp_path, monkeypatch):
+    import json
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("// a comment\n__global__ void k() { int x = 1; }  // trailing\n")
+    rec = {"w": {"dram_bytes_per_launch": 123, "sources": [str(src)], "capture": "c.md"}}
+    import hashlib
+    h = hashlib.sha256(bench._code_only(src.read_text()).encode()).hexdigest()
+    rec["w"]["sources_sha256"] = h
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.dram_traffic("w") == (123, "c.md")
+    assert bench.dram_traffic("other") == (None, None)
+    # a comment edit keeps the record, a code edit drops it
+    src.write_text("// another comment\n__global__ void k() { int x = 1; }\n")
+    assert bench.dram_traffic("w") == (123, "c.md")
+    src.write_text("__global__ void k() { int x = 2; }\n")
+    assert bench.dram_traffic("w")[0] is None
+
+
+def test_bench_counts_valid_slots_of_both_lists():
+    import bench
+    from sparse_mla_attention_03_gb300 import inputs
+    wl = inputs.make_dual_prefill("vs", T=3, H=8, ctx=256, topk=70, extra_ctx=128, extra_topk=40, seed=5,
+                                  ragged=True)
+    want = int(wl.topk_length.clamp(0, 70).sum()) + int(wl.extra_topk_length.clamp(0, 40).sum())
+    assert bench.valid_slots(wl) == want
+    w = bench.work_of(wl)
+    assert w["flops"] == 2.0 * 8 * (576 + 512) * want and w["gather_bytes"] == want * 656
