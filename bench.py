@@ -454,32 +454,42 @@ def cpu_baseline(parts_or_wls, budget_tokens, min_seconds=10.0, max_passes=12):
                       f"{t_tot:.1f} s)"}
 
 
-def run_reference(args):
-    """The CPU oracle as the reference arm: each step is a bounded token sample."""
+def run_reference(args, seconds=120.0):
+    """The CPU oracle as the reference arm.  Each step is a bounded token sample
+    of each part: its size is set from a calibration pass so that the timed
+    steps take about `seconds` in all, whatever --steps is (one process pool
+    serves every step)."""
     spec = workloads(args.tokens)[args.workload]
     wls = [mk(args.seed) for _, mk in spec["parts"]]
-    budget = args.ref_tokens
     cores = min(host_cores(), 32)
     times, toks = [], 0
-    for _ in range(args.warmup if args.warmup < 1 else 1):
+    with mp.get_context("spawn").Pool(cores, initializer=_pin_threads) as pool:
+        # calibration (also the warm-up): one token per process on each part
+        n_cal, t_cal = 0, 0.0
         for wl in wls:
-            oracle_time(wl, min(budget, cores), cores)
-    for _ in range(args.steps):
-        t = 0.0
-        for wl in wls:
-            n, dt = oracle_time(wl, budget, cores)
-            t += dt
-            toks += n
-        times.append(t)
+            n, dt = oracle_time(wl, cores, cores, pool)
+            n_cal += n
+            t_cal += dt
+        rate = n_cal / max(t_cal, 1e-9)  # tokens/s over the parts, all processes busy
+        per_part = int(rate * seconds / max(1, args.steps) / len(wls))
+        per_part = max(1, min(args.ref_tokens, per_part))
+        for _ in range(args.steps):
+            t = 0.0
+            for wl in wls:
+                n, dt = oracle_time(wl, per_part, cores, pool)
+                t += dt
+                toks += n
+            times.append(t)
     total = sum(times)
     value = toks / total
     return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy PCG64)",
-            "config": {"workload": spec["name"], "sample_tokens_per_part": budget},
+            "config": {"workload": spec["name"], "sample_tokens_per_part": per_part},
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"first {budget} tokens of each part per step"},
+                             "sample": f"first {per_part} tokens of each part per step, {args.steps} steps "
+                                       f"({total:.1f} s of oracle time)"},
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
