@@ -84,6 +84,26 @@ def test_decode_split_invariance_paged(H, S):
     assert_close(out, lse, *ref, tag=f"decode H={H} S={S}")
 
 
+@pytest.mark.parametrize("H,S", [(64, 0), (64, 5), (16, 0), (8, 3)])
+def test_paged_decode_ragged_lengths_and_padding(H, S):
+    # paged decode, 3 tokens per request, ragged topk_length (including 0 and
+    # the full width), -1 entries inside the valid range, one out-of-range
+    # logical page (masked and flagged)
+    wl = inputs.make_decode("decrag", n_req=3, tokens_per_req=3, H=H, ctx_per_req=4096, topk=700, seed=301 + S)
+    rng = np.random.default_rng(302)
+    lens = rng.integers(0, 701, size=wl.T)
+    lens[0], lens[1] = 0, 700
+    wl.topk_length = torch.from_numpy(lens.astype(np.int32))
+    idx = wl.indices.clone()
+    idx[2, 5:40] = -1
+    idx[3, 7] = 4096 + 64  # logical page 65 is outside the 64-column block-table row
+    wl.indices = idx
+    wl.topk_length[3] = 700
+    out, lse = run_decode(wl, num_splits=S)
+    assert_close(out, lse, *oracle_for(wl), tag=f"decode_ragged_H{H}_S{S}")
+    assert binding.get_error_word() & binding.ERRF_INDEX_RANGE
+
+
 def test_noncontiguous_views_written_in_place():
     # q[:, :8] / out[:, :8] views into width-64 buffers; index rows from a width-1024 buffer
     wl = inputs.make_prefill("views", T=6, H=8, ctx=2048, topk=192, seed=41, ld=1024)
