@@ -238,6 +238,7 @@ int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags);
  * input and output through args.
  *  - Calls whose partials need more than SMLA_NOALLOC_SCRATCH_BYTES (see
  *    sparse_mla_decode_workspace_size) are rejected with SMLA_ERR_INVALID.
+ *    A call that runs with one split has no partials and is never rejected.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, once per device); make that first call before any
  *    stream capture begins.

@@ -69,6 +69,16 @@ extern "C" int sparse_mla_decode_noalloc(const smla_args* a, int32_t num_splits,
   if ((rc = smla::host::setup_device(&dev)) != SMLA_OK) return rc;
   if (dev >= kMaxDev) return smla::host::set_error(SMLA_ERR_UNSUPPORTED, "device ordinal above 63");
   const int S = smla::host::decode_splits(a->T, a->H, a->topk, num_splits, smla::host::num_sms(dev));
+  smla::KParams p = smla::host::params_for(a, dev);
+  const int chunks = (a->topk + 63) / 64;
+  p.num_splits = S;
+  p.split_len = ((chunks + S - 1) / S) * 64;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (S == 1) {  // one split: final outputs straight from the attention kernel, no scratch
+    cudaError_t e = smla::launch_attention(p, st);
+    if (e != cudaSuccess) return smla::host::set_error(SMLA_ERR_CUDA, cudaGetErrorString(e));
+    return SMLA_OK;
+  }
   const size_t need = smla::host::decode_ws_bytes(a->T, a->H, S);
   if (need > (size_t)SMLA_NOALLOC_SCRATCH_BYTES) {
     char msg[320];
@@ -80,16 +90,6 @@ extern "C" int sparse_mla_decode_noalloc(const smla_args* a, int32_t num_splits,
   }
   void* scratch = nullptr;
   if ((rc = scratch_address(dev, &scratch)) != SMLA_OK) return rc;
-  smla::KParams p = smla::host::params_for(a, dev);
-  const int chunks = (a->topk + 63) / 64;
-  p.num_splits = S;
-  p.split_len = ((chunks + S - 1) / S) * 64;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (S == 1) {  // one split: final outputs straight from the attention kernel
-    cudaError_t e = smla::launch_attention(p, st);
-    if (e != cudaSuccess) return smla::host::set_error(SMLA_ERR_CUDA, cudaGetErrorString(e));
-    return SMLA_OK;
-  }
   // Every partial slot [t, h, s] is written by the split kernel before the
   // combine reads it (empty splits write lse = -inf), so nothing left in the
   // array by an earlier call needs clearing.

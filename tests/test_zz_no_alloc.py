@@ -45,6 +45,15 @@ def test_noalloc_decode_matches_workspace_decode_twice(cuda_lib):
                      tag=f"noalloc {wl.name}")
 
 
+def test_noalloc_single_split_needs_no_scratch(cuda_lib):
+    # one split writes the outputs directly: a size whose partials would not
+    # fit the built-in array still runs, and matches the workspace decode
+    wl = inputs.make_prefill("noalloc_s1", T=512, H=64, ctx=2048, topk=2048, seed=10)
+    assert binding.decode_workspace_size(wl.T, wl.H, wl.topk, 1) > binding.NOALLOC_SCRATCH_BYTES
+    ref, got = _both(wl, 1)
+    assert torch.equal(ref[0], got[0]) and torch.equal(ref[1], got[1])
+
+
 def test_noalloc_rejects_requests_beyond_the_array(cuda_lib):
     wl = inputs.make_prefill("noalloc_big", T=512, H=64, ctx=2048, topk=2048, seed=9, sink=None)
     need = binding.decode_workspace_size(wl.T, wl.H, wl.topk, 8)
