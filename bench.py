@@ -135,51 +135,109 @@ def load_peaks():
 
 
 # ------------------------------------------------------------------------------------------ oracle
-def _oracle_chunk(args):
+# The oracle runs in spawn processes that map each workload's arrays from
+# files written once (np.memmap, shared page cache): a timed call sends only
+# token numbers, so the measured rate is the oracle's, not the cost of
+# shipping a cache to every process.
+_WORKER = {}
+
+
+def _worker_init(spec):
+    import numpy as np
+    for key, fields in spec.items():
+        d = {}
+        for k, v in fields.items():
+            if isinstance(v, tuple) and len(v) == 4 and v[0] == "mmap":
+                d[k] = np.memmap(v[1], dtype=v[2], mode="r", shape=v[3])
+            else:
+                d[k] = v
+        _WORKER[key] = d
+
+
+def _oracle_job(args):
     import numpy as np
     import oracle.sparse_mla_oracle as O
-    (q, kv, idx, topk, sm, tl, sink, bt, tpr, toks, extra, fmt, layout) = args
-    if extra is None:
-        O.sparse_mla_forward(q, kv, idx, topk, sm, topk_length=tl, attn_sink=sink, block_table=bt,
-                             tokens_per_req=tpr, tokens=toks, q_selected=True, kv_format=fmt, layout=layout)
+    key, toks = args
+    w = _WORKER[key]
+    q = np.asarray(w["q"][toks], dtype=np.float64)
+    kw = dict(topk_length=w["topk_length"], attn_sink=w["attn_sink"], block_table=w["block_table"],
+              tokens_per_req=w["tokens_per_req"], tokens=toks, q_selected=True, kv_format=w["kv_format"],
+              layout=w["layout"])
+    if w["extra_kv"] is None:
+        O.sparse_mla_forward(q, w["kv"], w["indices"], w["topk"], w["sm_scale"], **kw)
     else:
-        kv2, idx2, topk2, tl2, bt2 = extra
-        O.sparse_mla_forward_dual(q, kv, idx, topk, kv2, idx2, topk2, sm, topk_length=tl, extra_topk_length=tl2,
-                                  attn_sink=sink, block_table=bt, extra_block_table=bt2, tokens_per_req=tpr,
-                                  tokens=toks, q_selected=True, kv_format=fmt, layout=layout)
+        O.sparse_mla_forward_dual(q, w["kv"], w["indices"], w["topk"], w["extra_kv"], w["extra_indices"],
+                                  w["extra_topk"], w["sm_scale"], extra_topk_length=w["extra_topk_length"],
+                                  extra_block_table=w["extra_block_table"], **kw)
     return len(toks)
 
 
-def oracle_time(wl, n_tokens, cores, pool=None):
-    """Oracle wall time on n_tokens tokens spread over `cores` spawn processes
-    (a pool of them is made here unless one is passed in)."""
-    import numpy as np
-    import torch
-    toks = np.arange(min(n_tokens, wl.T))
-    chunks = [c for c in np.array_split(toks, cores) if len(c)]
-    kv = wl.kv.numpy()
-    idx = wl.indices.numpy()
-    tl = None if wl.topk_length is None else wl.topk_length.numpy()
-    sink = None if wl.attn_sink is None else wl.attn_sink.numpy().astype(np.float64)
-    bt = None if wl.block_table is None else wl.block_table.numpy()
-    np_ = lambda x: None if x is None else x.numpy()
-    extra = (wl.extra_kv.numpy(), wl.extra_indices.numpy(), wl.extra_topk, np_(wl.extra_topk_length),
-             np_(wl.extra_block_table)) if wl.dual else None
-    jobs = [(wl.q[torch.as_tensor(c)].to(torch.float64).numpy(), kv, idx, wl.topk, wl.sm_scale, tl, sink, bt,
-             wl.tokens_per_req, c, extra, wl.kv_format, wl.layout) for c in chunks]
-    own = pool is None
-    if own:
-        pool = mp.get_context("spawn").Pool(cores, initializer=_pin_threads)
-    try:
-        pool.map(_oracle_chunk, jobs[:1])  # warm the workers' imports
+class OraclePool:
+    """A pool of `cores` spawn processes holding the given workloads (by name)."""
+
+    def __init__(self, wls, cores):
+        import shutil  # noqa: F401  (cleanup in close)
+        import numpy as np
+        import torch
+        self.cores = cores
+        self.dir = tempfile.mkdtemp(prefix="smla_oracle_")
+        spec = {}
+        for wl in wls:
+            fields = {}
+            for k in ("q", "kv", "indices", "topk_length", "attn_sink", "block_table", "extra_kv", "extra_indices",
+                      "extra_topk_length", "extra_block_table"):
+                t = getattr(wl, k)
+                if t is None:
+                    fields[k] = None
+                    continue
+                a = t.float().numpy() if t.dtype == torch.bfloat16 else t.numpy()
+                if k == "attn_sink":
+                    fields[k] = a.astype(np.float64)
+                    continue
+                path = os.path.join(self.dir, f"{len(spec)}_{k}.bin")
+                a = np.ascontiguousarray(a)
+                a.tofile(path)
+                fields[k] = ("mmap", path, a.dtype.str, a.shape)
+            fields.update(topk=wl.topk, extra_topk=wl.extra_topk, sm_scale=wl.sm_scale,
+                          tokens_per_req=wl.tokens_per_req, kv_format=wl.kv_format, layout=wl.layout)
+            spec[wl.name] = fields
+        self.T = {wl.name: wl.T for wl in wls}
+        # one BLAS thread per process: the children read these at start-up,
+        # before anything (the unpickled arguments included) loads numpy
+        keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+        saved = {k: os.environ.get(k) for k in keys}
+        os.environ.update({k: "1" for k in keys})
+        try:
+            self.pool = mp.get_context("spawn").Pool(cores, initializer=_worker_init, initargs=(spec,))
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        for wl in wls:  # warm the workers' imports and mappings (untimed)
+            self.pool.map(_oracle_job, [(wl.name, np.arange(1))] * cores)
+
+    def time(self, name, n_tokens):
+        """Oracle wall time on the first n_tokens tokens of workload `name`."""
+        import numpy as np
+        toks = np.arange(min(n_tokens, self.T[name]))
+        jobs = [(name, c) for c in np.array_split(toks, self.cores) if len(c)]
         t0 = time.perf_counter()
-        n = sum(pool.map(_oracle_chunk, jobs))
-        dt = time.perf_counter() - t0
-    finally:
-        if own:
-            pool.close()
-            pool.join()
-    return n, dt
+        n = sum(self.pool.map(_oracle_job, jobs))
+        return n, time.perf_counter() - t0
+
+    def close(self):
+        import shutil
+        self.pool.close()
+        self.pool.join()
+        shutil.rmtree(self.dir, ignore_errors=True)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
 
 
 def _pin_threads():
@@ -294,6 +352,111 @@ def make_call(kind, binding, d, wl, out, lse, ws, num_splits):
     return call
 
 
+def prepare_parts(spec, seed, dev, num_splits):
+    """Device copies, outputs and the call of every part of a workload."""
+    import torch
+    from sparse_mla_attention_03_gb300 import binding
+    parts = []
+    for tag, mk in spec["parts"]:
+        wl = mk(seed)
+        d = {k: (None if getattr(wl, k) is None else getattr(wl, k).to(dev))
+             for k in ("q", "kv", "indices", "topk_length", "attn_sink", "block_table", "extra_kv",
+                       "extra_indices", "extra_topk_length", "extra_block_table")}
+        out = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device=dev)
+        ws = None
+        launches = 1  # kernels per call: the attention kernel, plus the combine when decode splits
+        splits = None
+        if spec["kind"] != "prefill":
+            width = binding.dual_width(wl.topk, wl.extra_topk) if wl.dual else wl.topk
+            ws = torch.empty(max(256, binding.decode_workspace_size(wl.T, wl.H, width, num_splits)),
+                             dtype=torch.uint8, device=dev)
+            splits = binding.decode_num_splits(wl.T, wl.H, width, num_splits)
+            launches = 1 if splits == 1 else 2
+        call = make_call(spec["kind"], binding, d, wl, out, lse, ws, num_splits)
+        parts.append(dict(tag=tag, wl=wl, d=d, out=out, lse=lse, ws=ws, call=call, work=work_of(wl),
+                          launches=launches, splits=splits))
+    return parts
+
+
+def time_parts(parts, steps, warmup, flush, stream, barrier):
+    """Per-part CUDA-event times (ms) of `steps` timed steps after `warmup`
+    untimed ones; the L2 is flushed (a write larger than L2) before each step."""
+    import torch
+    for _ in range(warmup):
+        for p in parts:
+            p["call"]()
+    barrier()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
+          for _ in range(steps)]
+    barrier()
+    for s in range(steps):
+        flush.fill_(s & 0xFF)
+        for j, p in enumerate(parts):
+            ev[s][j][0].record(stream)
+            p["call"]()
+            ev[s][j][1].record(stream)
+    barrier()
+    return [[ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(steps)] for j in range(len(parts))]
+
+
+def roofline_of(bound, work, ms, peaks, workload):
+    """Roofline entry of one kernel launch set: algorithmic flops (tensor-bound
+    paths) or bytes (gather/HBM-bound paths) per launch over its measured time,
+    against the measured peak; `traffic` is the ncu DRAM bytes per launch when
+    a capture of the current kernel sources exists (and the DRAM rate it gives)."""
+    sec = ms / 1e3
+    if bound == "tensor":
+        achieved = work["flops"] / sec / 1e12
+        r = dict(bound="tensor", achieved=round(achieved, 2), peak=peaks["tflops"], unit="TFLOP/s",
+                 frac=round(achieved / peaks["tflops"], 4), traffic=None,
+                 peak_source=f"{peaks['src']} bf16 dense burst (fp16 operands run at the same rate)")
+    else:
+        achieved = work["bytes"] / sec / 1e9
+        r = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm"], unit="GB/s",
+                 frac=round(achieved / peaks["hbm"], 4), traffic=None,
+                 peak_source=f"{peaks['src']} HBM copy bandwidth",
+                 achieved_kind="algorithmic bytes (gather + q/out/lse/indices) per launch / time")
+    traffic, src = dram_traffic(workload)
+    if traffic is not None:
+        r["traffic"] = traffic
+        r["traffic_unit"] = "bytes per launch (mean), ncu dram__bytes_read.sum + dram__bytes_write.sum"
+        r["dram_gbs"] = round(traffic / sec / 1e9, 1)
+        r["dram_frac"] = round(traffic / sec / 1e9 / peaks["hbm"], 4)
+    if src is not None:
+        r["traffic_source"] = src
+    return r
+
+
+# The other workloads, timed in the same run and with the same protocol as
+# the headline one (rank 0's numbers).
+PER_CONFIG = ("fewhead", "decode", "large", "dual_decode", "prefill16k_int8")
+
+
+def run_per_config(args, dev, stream, barrier, flush, peaks, l2_bytes):
+    import torch
+    res = {}
+    for key in PER_CONFIG:
+        if key == args.workload:
+            continue
+        spec = workloads(None)[key]
+        parts = prepare_parts(spec, args.seed, dev, args.num_splits)
+        ms_lists = time_parts(parts, max(3, min(args.steps, 50)), args.warmup, flush, stream, barrier)
+        ms = sum(statistics.median(m) for m in ms_lists)
+        work = {k: sum(p["work"][k] for p in parts) for k in ("flops", "bytes", "valid")}
+        tokens = sum(p["wl"].T for p in parts)
+        cache = sum(p["wl"].kv.numel() + (p["wl"].extra_kv.numel() if p["wl"].dual else 0) for p in parts)
+        e = dict(workload=spec["name"], ms=round(ms, 4), query_tokens_per_s=round(tokens / (ms / 1e3), 1),
+                 roofline=roofline_of(spec["bound"], work, ms, peaks, key), cache_bytes=cache,
+                 cache_in_l2=bool(cache <= l2_bytes), gpu_launches_per_step=sum(p["launches"] for p in parts))
+        if parts[0]["splits"] is not None:
+            e["num_splits"] = parts[0]["splits"]
+        res[key] = e
+        del parts
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from sparse_mla_attention_03_gb300 import binding
@@ -303,26 +466,7 @@ def run_ours(args, rank, world, local_rank):
     binding.load()
     spec = workloads(args.tokens)[args.workload]
     peaks = load_peaks()
-    parts = []
-    for tag, mk in spec["parts"]:
-        wl = mk(rank_seed(args.seed, rank))
-        d = {k: (None if getattr(wl, k) is None else getattr(wl, k).to(dev))
-             for k in ("q", "kv", "indices", "topk_length", "attn_sink", "block_table", "extra_kv",
-                       "extra_indices", "extra_topk_length", "extra_block_table")}
-        out = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, device=dev)
-        lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device=dev)
-        ws = None
-        if spec["kind"] != "prefill":
-            width = binding.dual_width(wl.topk, wl.extra_topk) if wl.dual else wl.topk
-            ws = torch.empty(max(256, binding.decode_workspace_size(wl.T, wl.H, width, args.num_splits)),
-                             dtype=torch.uint8, device=dev)
-        call = make_call(spec["kind"], binding, d, wl, out, lse, ws, args.num_splits)
-        # kernels per call: the attention kernel, plus the combine when decode splits
-        launches = 1
-        if spec["kind"] != "prefill":
-            launches = 1 if binding.decode_num_splits(wl.T, wl.H, width, args.num_splits) == 1 else 2
-        parts.append(dict(tag=tag, wl=wl, d=d, out=out, lse=lse, ws=ws, call=call, work=work_of(wl),
-                          launches=launches))
+    parts = prepare_parts(spec, rank_seed(args.seed, rank), dev, args.num_splits)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -331,49 +475,18 @@ def run_ours(args, rank, world, local_rank):
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    for _ in range(args.warmup):
-        for p in parts:
-            p["call"]()
-    barrier()
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
-          for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
-        barrier()
         t0 = time.perf_counter()
-        for s in range(args.steps):
-            flush.fill_(s & 0xFF)
-            for j, p in enumerate(parts):
-                ev[s][j][0].record(stream)
-                p["call"]()
-                ev[s][j][1].record(stream)
-        barrier()
+        per_part_ms = time_parts(parts, args.steps, args.warmup, flush, stream, barrier)
         wall = time.perf_counter() - t0
-    per_part_ms = [[ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps)] for j in range(len(parts))]
     step_ms = [sum(per_part_ms[j][s] for j in range(len(parts))) for s in range(args.steps)]
     total_ms = global_elapsed_ms(sum(step_ms), world, dev)
     tokens_per_step = sum(p["wl"].T for p in parts)
     value = job_throughput(tokens_per_step, args.steps, world, total_ms)
 
     # roofline of the dominant kernel (the attention kernel; for decode the split kernel dominates)
-    flops = sum(p["work"]["flops"] for p in parts)
-    nbytes = sum(p["work"]["bytes"] for p in parts)
-    avg_step_s = total_ms / args.steps / 1e3
-    if spec["bound"] == "tensor":
-        achieved = flops / avg_step_s / 1e12
-        roof = dict(bound="tensor", achieved=round(achieved, 2), peak=peaks["tflops"], unit="TFLOP/s",
-                    frac=round(achieved / peaks["tflops"], 4), traffic=None,
-                    peak_source=f"{peaks['src']} bf16 dense burst (fp16 operands run at the same rate)")
-    else:
-        achieved = nbytes / avg_step_s / 1e9
-        roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm"], unit="GB/s",
-                    frac=round(achieved / peaks["hbm"], 4), traffic=None,
-                    peak_source=f"{peaks['src']} HBM copy bandwidth")
-    traffic, src = dram_traffic(args.workload)
-    if traffic is not None:
-        roof["traffic"] = traffic
-        roof["traffic_unit"] = "bytes per launch (mean), ncu dram__bytes_read.sum + dram__bytes_write.sum"
-    if src is not None:
-        roof["traffic_source"] = src
+    work = {k: sum(p["work"][k] for p in parts) for k in ("flops", "bytes", "valid")}
+    roof = roofline_of(spec["bound"], work, total_ms / args.steps, peaks, args.workload)
     roof["per_launch"] = {p["tag"]: dict(ms=round(statistics.mean(per_part_ms[j]), 4),
                                          tflops=round(p["work"]["flops"] / (statistics.mean(per_part_ms[j]) / 1e3) / 1e12, 2),
                                          gbs=round(p["work"]["bytes"] / (statistics.mean(per_part_ms[j]) / 1e3) / 1e9, 1))
@@ -397,6 +510,11 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk.summary(),
         "wall_s": round(wall, 3),
     }
+    if not args.no_per_config and rank == 0:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        # rank 0 alone: a local barrier (no collective the other ranks would miss)
+        line["per_config"] = run_per_config(args, dev, stream, lambda: torch.cuda.synchronize(dev), flush, peaks,
+                                            l2)
     return line, parts
 
 
@@ -462,61 +580,73 @@ def run_e2e(args, parts, dev, stream, world):
             "pipelined": "H2D of step s+1 and D2H of step s-1 overlap the kernels of step s (3 streams)"}
 
 
-def cpu_baseline(parts_or_wls, budget_tokens, min_seconds=10.0, max_passes=12):
-    """The oracle timed on the first budget_tokens tokens of each part, repeated
-    until about min_seconds of CPU work have been measured (bounded passes)."""
+# One sampling protocol for both CPU numbers (cpu_baseline and the reference
+# arm): the oracle on the first ORACLE_SAMPLE tokens of each part per pass,
+# spread over the host's cores, passes repeated to a time budget.
+ORACLE_SAMPLE = 256
+
+
+def oracle_rate(wls, seconds, max_passes=50, min_passes=1, pool=None):
+    """Tokens/s of the oracle over `wls`, timed pass by pass (one pass = the
+    first ORACLE_SAMPLE tokens of every part) until `seconds` of oracle time."""
     cores = min(host_cores(), 32)
-    n_tot, t_tot, passes = 0, 0.0, 0
-    descs = []
-    with mp.get_context("spawn").Pool(cores, initializer=_pin_threads) as pool:
-        while passes < max_passes and (passes == 0 or t_tot < min_seconds):
-            for wl in parts_or_wls:
-                n, dt = oracle_time(wl, budget_tokens, cores, pool)
+    own = pool is None
+    if own:
+        pool = OraclePool(wls, cores)
+    try:
+        n_tot, t_tot, passes, per_pass = 0, 0.0, 0, []
+        while passes < max_passes and (passes < min_passes or t_tot < seconds):
+            t_pass = 0.0
+            for wl in wls:
+                n, dt = pool.time(wl.name, ORACLE_SAMPLE)
                 n_tot += n
-                t_tot += dt
-                if passes == 0:
-                    descs.append(f"{wl.name}: first {n} tokens")
+                t_pass += dt
+            per_pass.append(t_pass)
+            t_tot += t_pass
             passes += 1
-    return {"value": round(n_tot / t_tot, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "; ".join(descs) + f", {passes} passes (fp64 numpy oracle, {cores} spawn processes, "
-                      f"{t_tot:.1f} s)"}
+    finally:
+        if own:
+            pool.close()
+    return dict(value=n_tot / t_tot, cores=cores, passes=passes, seconds=t_tot, per_pass=per_pass,
+                tokens_per_pass=sum(min(ORACLE_SAMPLE, wl.T) for wl in wls))
 
 
-def run_reference(args, seconds=120.0):
-    """The CPU oracle as the reference arm.  Each step is a bounded token sample
-    of each part: its size is set from a calibration pass so that the timed
-    steps take about `seconds` in all, whatever --steps is (one process pool
-    serves every step)."""
+def cpu_baseline(wls, seconds=10.0):
+    r = oracle_rate(wls, seconds)
+    return {"value": round(r["value"], 2), "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+            "sample": f"first {ORACLE_SAMPLE} tokens of each of {', '.join(wl.name for wl in wls)} per pass, "
+                      f"{r['passes']} passes (fp64 numpy oracle, {r['cores']} spawn processes, "
+                      f"{r['seconds']:.1f} s)"}
+
+
+def run_reference(args, seconds=60.0):
+    """The CPU oracle as the reference arm: each step is one pass of the same
+    sample as cpu_baseline (the first ORACLE_SAMPLE tokens of each part),
+    after --warmup untimed passes; --steps is capped so that the run stays
+    within a few minutes (the line says how many steps ran)."""
     spec = workloads(args.tokens)[args.workload]
     wls = [mk(args.seed) for _, mk in spec["parts"]]
     cores = min(host_cores(), 32)
-    times, toks = [], 0
-    with mp.get_context("spawn").Pool(cores, initializer=_pin_threads) as pool:
-        # calibration (also the warm-up): one token per process on each part
-        n_cal, t_cal = 0, 0.0
-        for wl in wls:
-            n, dt = oracle_time(wl, cores, cores, pool)
-            n_cal += n
-            t_cal += dt
-        rate = n_cal / max(t_cal, 1e-9)  # tokens/s over the parts, all processes busy
-        per_part = int(rate * seconds / max(1, args.steps) / len(wls))
-        per_part = max(1, min(args.ref_tokens, per_part))
-        for _ in range(args.steps):
-            t = 0.0
+    with OraclePool(wls, cores) as pool:
+        for _ in range(min(args.warmup, 3)):
             for wl in wls:
-                n, dt = oracle_time(wl, per_part, cores, pool)
-                t += dt
-                toks += n
-            times.append(t)
-    total = sum(times)
+                pool.time(wl.name, ORACLE_SAMPLE)
+        first = oracle_rate(wls, 0.0, max_passes=1, pool=pool)
+        steps = max(1, min(args.steps, int(seconds / max(first["seconds"], 1e-6))))
+        r = oracle_rate(wls, float("inf"), max_passes=steps - 1, min_passes=steps - 1, pool=pool) \
+            if steps > 1 else None
+    per_pass = first["per_pass"] + (r["per_pass"] if r else [])
+    total = sum(per_pass)
+    toks = first["tokens_per_pass"] * len(per_pass)
     value = toks / total
     return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
+            "steps": len(per_pass), "warmup": args.warmup, "ms_per_step": round(total / len(per_pass) * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy PCG64)",
-            "config": {"workload": spec["name"], "sample_tokens_per_part": per_part},
+            "config": {"workload": spec["name"], "sample_tokens_per_part": ORACLE_SAMPLE,
+                       "steps_requested": args.steps},
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"first {per_part} tokens of each part per step, {args.steps} steps "
+                             "sample": f"first {ORACLE_SAMPLE} tokens of each part per step, {len(per_pass)} steps "
                                        f"({total:.1f} s of oracle time)"},
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -532,9 +662,9 @@ def main():
                     default="prefill16k")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-tokens", type=int, default=512, help="oracle sample per part for cpu_baseline")
-    ap.add_argument("--ref-tokens", type=int, default=128, help="oracle sample per part per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the selected workload (skip the other workloads' entries)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="query tokens of a prefill workload (smaller profiling case; default: the full workload)")
     args = ap.parse_args()
@@ -556,7 +686,7 @@ def main():
         if args.no_cpu_baseline:
             line["cpu_baseline"] = None
         else:
-            line["cpu_baseline"] = cpu_baseline([p["wl"] for p in parts], args.cpu_tokens)
+            line["cpu_baseline"] = cpu_baseline([p["wl"] for p in parts])
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch

@@ -207,8 +207,28 @@ int sparse_mla_decode(const smla_args* args, int32_t num_splits, void* workspace
 size_t sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t topk,
                                         int32_t num_splits);
 
-/* The split count sparse_mla_decode uses for num_splits (0 = automatic). */
+/*
+ * The split count sparse_mla_decode uses for num_splits (0 = automatic).
+ * The automatic choice minimises (CTA waves) x (per-CTA fixed cost + its
+ * share of the 64-slot chunks) for the kernel that will run, and applies the
+ * L2-footprint guard of FlashInfer PR #4802 (commit note on the analytical
+ * cpb model: min(G, S) * cpb * W must fit in L2): when a token's rows are
+ * gathered by more than one CTA (head groups of 64, or of the warp-MMA
+ * kernel's width), split counts are not chosen whose rows streamed between a
+ * row's first and last reader -- min(G, resident CTAs) x chunks per CTA x 64
+ * rows x 656 bytes, G being the span of CTAs from the first reader to the
+ * last, (head groups - 1) x splits + 1 in this grid's order -- exceed the
+ * device's L2, unless none fits.  Returns 0 for invalid sizes.
+ */
 int32_t sparse_mla_decode_num_splits(int32_t T, int32_t H, int32_t topk, int32_t num_splits);
+
+/*
+ * The same choice for a device described by its SM count and L2 size in
+ * bytes instead of the current one (host only: no CUDA call).  Returns 0 for
+ * invalid sizes.
+ */
+int32_t sparse_mla_plan_num_splits(int32_t T, int32_t H, int32_t topk, int32_t num_splits, int32_t num_sms,
+                                   int64_t l2_bytes);
 
 /*
  * Index handling only: rows_out[t*rows_stride_t + j] (int32, device) receives
@@ -226,6 +246,22 @@ int sparse_mla_resolve_rows(const smla_args* args, int32_t* rows_out, int64_t ro
 int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags);
 
 /*
+ * Limit, in nanoseconds of GPU global time, of every bounded in-kernel wait
+ * of the calls made after it, on any thread (default 1000000000, one
+ * second).  Returns the previous limit.  Every wait of the tcgen05 kernel on
+ * an mbarrier is bounded, so that a pipeline stage that never completes ends
+ * the CTA with an error status instead of a hang (FlashInfer PR #4802 page,
+ * follow-up fix note on the DGX Spark hang: IO warps that no barrier counted
+ * spun forever on mbarrier_wait_parity).  When a limit runs out, the CTA sets
+ * SMLA_ERRF_TIMEOUT, stops every role, waits for its issued MMAs, frees its
+ * tensor memory and returns without writing its outputs; the context stays
+ * usable.  A limit of 0 makes the first wait that does not succeed at once
+ * give up: a test hook for that path.  The limit in force is read when a call
+ * is made; calls already queued keep theirs.
+ */
+uint64_t sparse_mla_set_wait_limit_ns(uint64_t ns);
+
+/*
  * Decode without any device allocation -- no counterpart on the pages; added
  * for callers that cannot allocate device memory: a host engine that owns all
  * device memory through its own pool and gives a library only tensors and a
@@ -236,8 +272,11 @@ int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags);
  * into the library (SMLA_NOALLOC_SCRATCH_BYTES per GPU, kept by every GPU
  * that loads it until the process exits).  The caller still passes every
  * input and output through args.
- *  - Calls whose partials need more than SMLA_NOALLOC_SCRATCH_BYTES (see
- *    sparse_mla_decode_workspace_size) are rejected with SMLA_ERR_INVALID.
+ *  - With num_splits == 0 the split count is the automatic choice lowered,
+ *    if needed, to the largest count whose partials fit the array; such a
+ *    call is never rejected for its size.  An explicit num_splits whose
+ *    partials need more than SMLA_NOALLOC_SCRATCH_BYTES (see
+ *    sparse_mla_decode_workspace_size) is rejected with SMLA_ERR_INVALID.
  *    A call that runs with one split has no partials and is never rejected.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, once per device); make that first call before any
@@ -249,6 +288,9 @@ int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags);
  */
 #define SMLA_NOALLOC_SCRATCH_BYTES (64u << 20)
 int sparse_mla_decode_noalloc(const smla_args* args, int32_t num_splits, smla_stream_t stream);
+
+/* Size in bytes of the no-alloc decode's built-in array, as compiled. */
+size_t sparse_mla_noalloc_scratch_bytes(void);
 
 /*
  * Dual-cache form: one softmax over the candidates of two index lists, each

@@ -69,8 +69,11 @@ SYMBOLS = {
     "sparse_mla_decode": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "sparse_mla_decode_workspace_size": (ctypes.c_size_t, [ctypes.c_int32] * 4),
     "sparse_mla_decode_num_splits": (ctypes.c_int32, [ctypes.c_int32] * 4),
+    "sparse_mla_plan_num_splits": (ctypes.c_int32, [ctypes.c_int32] * 5 + [ctypes.c_int64]),
     "sparse_mla_resolve_rows": (ctypes.c_int, [_P, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
     "sparse_mla_decode_noalloc": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_void_p]),
+    "sparse_mla_noalloc_scratch_bytes": (ctypes.c_size_t, []),
+    "sparse_mla_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "sparse_mla_get_error_word": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "sparse_mla_last_error": (ctypes.c_char_p, []),
     "sparse_mla_abi_version": (ctypes.c_int32, []),
@@ -214,6 +217,11 @@ def decode_num_splits(T, H, topk, num_splits=0) -> int:
     return int(load().sparse_mla_decode_num_splits(T, H, topk, num_splits))
 
 
+def plan_num_splits(T, H, topk, num_splits, num_sms, l2_bytes) -> int:
+    """The split count for a device with ``num_sms`` SMs and ``l2_bytes`` of L2 (host only)."""
+    return int(load().sparse_mla_plan_num_splits(T, H, topk, num_splits, num_sms, l2_bytes))
+
+
 def sparse_mla_decode(q, kv, indices, sm_scale, topk=None, topk_length=None, attn_sink=None,
                       block_table=None, tokens_per_req=1, num_splits=0, workspace=None, out=None,
                       lse=None, stream=None,
@@ -235,7 +243,15 @@ def sparse_mla_decode(q, kv, indices, sm_scale, topk=None, topk_length=None, att
     return out, lse
 
 
-NOALLOC_SCRATCH_BYTES = 64 << 20
+def noalloc_scratch_bytes() -> int:
+    """Size of the no-alloc decode's built-in array, read from the library."""
+    return int(load().sparse_mla_noalloc_scratch_bytes())
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of every bounded in-kernel wait of later calls; returns the previous one."""
+    return int(load().sparse_mla_set_wait_limit_ns(int(ns)))
+
 
 
 def sparse_mla_decode_noalloc(q, kv, indices, sm_scale, topk=None, topk_length=None, attn_sink=None,

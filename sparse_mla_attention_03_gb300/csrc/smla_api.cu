@@ -4,6 +4,9 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
+#include <atomic>
 #include <mutex>
 
 #include "../../include/sparse_mla.h"
@@ -12,6 +15,16 @@
 namespace {
 
 thread_local char g_last_error[512] = "";
+
+// Limit of every bounded in-kernel wait, for the calls that follow.
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+
+// One NVTX range per entry point (named after it), for profiler timelines.
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+};
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -129,6 +142,8 @@ smla::KParams make_params(const smla_args* a, int dev) {
   // meet with L2 prefetch and earlier register loads.
   p.big_cache = (int64_t)a->num_pages * SMLA_PAGE * SMLA_ROW_BYTES > g_l2_bytes[dev] / 4 ? 1 : 0;
   p.err = g_err_ptr[dev];
+  p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  p.cta_slots = g_num_sms[dev];
   p.kv_format = a->kv_format;
   p.nope = a->layout == SMLA_LAYOUT_NOPE ? 1 : 0;
   // one list: the second-list fields stay inert
@@ -194,51 +209,84 @@ smla::KParams make_params_dual(const smla_args* a, const smla_extra_args* x, int
 
 // Decode split choice.  An explicit request is honoured up to the number of
 // 64-slot chunks; the automatic choice minimises waves x CTA length for the
-// kernel that will run (measured against split sweeps on GB300).
-int splits_for(int T, int H, int topk, int num_splits, int num_sms) {
-  const int chunks = (topk + 63) / 64;
-  int S;
-  if (num_splits > 0) {
-    S = num_splits < chunks ? num_splits : chunks;
-  } else if (smla::tc_supported(H)) {
+// kernel that will run (measured against split sweeps on GB300), subject to
+// an L2-footprint guard.
+//
+// The guard (FlashInfer PR #4802, commit note on the analytical cpb model:
+// the "L2-footprint guard rail" over min(G, S) * cpb * W): when the rows of a
+// token are gathered by more than one CTA (one per head group, R > 1), the
+// later readers find them in L2 only while the rows streamed between the
+// first and the last read -- min(G, resident CTA slots) x 64-slot chunks per
+// CTA x 64 rows x 656 bytes -- fit in L2.  Split counts beyond it are
+// excluded; if none fits, the unconstrained pick stands.  G is the span of
+// CTAs, in dispatch order, from a row's first reader to its last: this grid
+// numbers the head-group CTAs of one (token, split) S apart, so G = (R-1) S
+// + 1 and all readers of a row normally run at the same time.  (Taking G as
+// the whole grid, as for a kernel whose readers are a grid apart, moved H=128
+// decode on GB300 from one split to two, measured 19-24% slower.)  With one
+// CTA per token and split (R == 1) no row is read twice and the guard does
+// not apply.
+constexpr double kChunkBytes = 64.0 * SMLA_ROW_BYTES;
+
+struct SplitModel {
+  int64_t base;     // CTAs per split: tokens x head-group CTAs per token
+  int64_t slots;    // resident CTA slots: SMs x CTAs per SM
+  int rereads;      // CTAs that gather the same rows (head groups per token)
+  double fixed;     // per-CTA fixed cost, in chunk units
+  double per_chunk; // cost of one 64-slot chunk
+  bool tile128;     // cost in 128-slot tiles (tcgen05 kernel): (chunks + 1) / 2
+  double merge;     // cost per split of the combine's merge
+};
+
+SplitModel split_model(int H, int num_sms) {
+  const int sms = num_sms > 0 ? num_sms : 148;
+  SplitModel m;
+  if (smla::tc_supported(H)) {
     // tcgen05 kernel: one CTA per SM, each paying a fixed cost (q load, first
     // gather latency, epilogue: about 2.5 tiles' worth) plus one unit per
-    // 128-row tile.  Pick the split count with the fewest waves x CTA length.
-    const int sms = num_sms > 0 ? num_sms : 148;
-    const int64_t base = (int64_t)T * (H / 64);
-    double best = 0.0;
-    S = 1;
+    // 128-row tile
+    m = SplitModel{H / 64, sms, H / 64, 2.5, 1.0, true, 0.0};
+  } else {
+    // warp-MMA kernel: a wave of SMs x resident CTAs (4 per SM for 8-head
+    // CTAs, 2 for 16-head CTAs), a fixed cost of about 1.5 64-slot chunks, one
+    // unit per chunk, and 0.05 units per split for the combine's merge
+    const int hpc = smla::heads_per_cta(H);
+    const int groups = (H + hpc - 1) / hpc;
+    m = SplitModel{groups, (int64_t)sms * (hpc == 8 ? 4 : 2), groups, 1.5, 1.0, false, 0.05};
+  }
+  return m;
+}
+
+int splits_for(int T, int H, int topk, int num_splits, int num_sms, int64_t l2_bytes) {
+  const int chunks = (topk + 63) / 64;
+  int S = 1;
+  if (num_splits > 0) {
+    S = num_splits < chunks ? num_splits : chunks;
+  } else {
+    const SplitModel m = split_model(H, num_sms);
+    const int64_t base = (int64_t)T * m.base;
+    double best_any = 0.0, best_fit = 0.0;
+    int s_any = 1, s_fit = 0;
     for (int s = 1; s <= SMLA_MAX_SPLITS && s <= chunks; ++s) {
-      const int per = (chunks + s - 1) / s;               // 64-slot chunks per split
+      const int per = (chunks + s - 1) / s;                 // 64-slot chunks per split
       if (s > 1 && (chunks + per - 1) / per < s) continue;  // same partition as a smaller s
       const int64_t ctas = base * s;
-      const double waves = (double)((ctas + sms - 1) / sms);
-      const double cost = waves * (2.5 + (per + 1) / 2);
-      if (s == 1 || cost < best * 0.97) {
-        best = cost;
-        S = s;
+      const double waves = (double)((ctas + m.slots - 1) / m.slots);
+      const double len = m.tile128 ? (double)((per + 1) / 2) : (double)per * m.per_chunk;
+      const double cost = waves * (m.fixed + len) + m.merge * s;
+      if (s == 1 || cost < best_any * 0.97) {
+        best_any = cost;
+        s_any = s;
+      }
+      const int64_t span = (int64_t)(m.rereads - 1) * s + 1;  // CTAs from a row's first reader to its last
+      const double footprint = (double)(span < m.slots ? span : m.slots) * per * kChunkBytes;
+      const bool fits = m.rereads <= 1 || l2_bytes <= 0 || footprint <= (double)l2_bytes;
+      if (fits && (s_fit == 0 || cost < best_fit * 0.97)) {
+        best_fit = cost;
+        s_fit = s;
       }
     }
-  } else {
-    // warp-MMA kernel: the same waves x CTA-length model, with a wave of
-    // SMs x resident CTAs (4 per SM for 8-head CTAs, 2 for 16-head CTAs), a
-    // fixed cost of about 1.5 64-slot chunks, one unit per chunk, and 0.05
-    // units per split for the combine's merge
-    const int hpc = smla::heads_per_cta(H);
-    const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 148) * (hpc == 8 ? 4 : 2);
-    const int64_t base = (int64_t)T * ((H + hpc - 1) / hpc);
-    double best = 0.0;
-    S = 1;
-    for (int s = 1; s <= SMLA_MAX_SPLITS && s <= chunks; ++s) {
-      const int per = (chunks + s - 1) / s;
-      if (s > 1 && (chunks + per - 1) / per < s) continue;
-      const double waves = (double)((base * s + cap - 1) / cap);
-      const double cost = waves * (1.5 + per) + 0.05 * s;
-      if (s == 1 || cost < best * 0.97) {
-        best = cost;
-        S = s;
-      }
-    }
+    S = s_fit > 0 ? s_fit : s_any;
   }
   if (S < 1) S = 1;
   // effective count: chunks per split rounded up, then splits that hold slots
@@ -256,7 +304,7 @@ size_t ws_bytes(int64_t T, int64_t H, int64_t S) {
 // combined width of the dual-cache form).
 int decode_launch(smla::KParams p, int width, int num_splits, void* workspace, size_t workspace_bytes,
                   smla_stream_t stream, int dev) {
-  const int S = splits_for(p.T, p.H, width, num_splits, g_num_sms[dev]);
+  const int S = splits_for(p.T, p.H, width, num_splits, g_num_sms[dev], g_l2_bytes[dev]);
   const size_t need = ws_bytes(p.T, p.H, S);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(SMLA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
@@ -286,12 +334,15 @@ int decode_launch(smla::KParams p, int width, int num_splits, void* workspace, s
 
 extern "C" {
 
-int32_t sparse_mla_abi_version(void) { return 4; }
+int32_t sparse_mla_abi_version(void) { return 5; }
+
+uint64_t sparse_mla_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
 
 const char* sparse_mla_last_error(void) { return g_last_error; }
 
 int sparse_mla_prefill(const smla_args* a, smla_stream_t stream) {
   g_last_error[0] = 0;
+  Range range("sparse_mla_prefill");
   int rc = validate(a);
   if (rc != SMLA_OK) return rc;
   if (a->T == 0) return SMLA_OK;
@@ -303,15 +354,25 @@ int sparse_mla_prefill(const smla_args* a, smla_stream_t stream) {
   return SMLA_OK;
 }
 
+int32_t sparse_mla_plan_num_splits(int32_t T, int32_t H, int32_t topk, int32_t num_splits, int32_t num_sms,
+                                   int64_t l2_bytes) {
+  if (T < 0 || H < 1 || H > SMLA_MAX_HEADS || topk < 1 || num_splits < 0 || num_splits > SMLA_MAX_SPLITS ||
+      num_sms < 1 || l2_bytes < 0)
+    return 0;
+  return splits_for(T, H, topk, num_splits, num_sms, l2_bytes);
+}
+
 int32_t sparse_mla_decode_num_splits(int32_t T, int32_t H, int32_t topk, int32_t num_splits) {
   if (T < 0 || H < 1 || H > SMLA_MAX_HEADS || topk < 1 || num_splits < 0 || num_splits > SMLA_MAX_SPLITS) return 0;
   int sms = 0;
+  int64_t l2 = 0;
   if (num_splits == 0) {
     int dev;
     if (device_setup(&dev) != SMLA_OK) return 0;
     sms = g_num_sms[dev];
+    l2 = g_l2_bytes[dev];
   }
-  return splits_for(T, H, topk, num_splits, sms);
+  return splits_for(T, H, topk, num_splits, sms, l2);
 }
 
 size_t sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t topk, int32_t num_splits) {
@@ -324,6 +385,7 @@ size_t sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t topk, int3
 int sparse_mla_decode(const smla_args* a, int32_t num_splits, void* workspace, size_t workspace_bytes,
                       smla_stream_t stream) {
   g_last_error[0] = 0;
+  Range range("sparse_mla_decode");
   int rc = validate(a);
   if (rc != SMLA_OK) return rc;
   if (num_splits < 0 || num_splits > SMLA_MAX_SPLITS)
@@ -341,6 +403,7 @@ int32_t sparse_mla_dual_width(int32_t topk, int32_t extra_topk) {
 
 int sparse_mla_prefill_dual(const smla_args* a, const smla_extra_args* x, smla_stream_t stream) {
   g_last_error[0] = 0;
+  Range range("sparse_mla_prefill_dual");
   int rc = validate(a);
   if (rc != SMLA_OK) return rc;
   if ((rc = validate_extra(a, x)) != SMLA_OK) return rc;
@@ -356,6 +419,7 @@ int sparse_mla_prefill_dual(const smla_args* a, const smla_extra_args* x, smla_s
 int sparse_mla_decode_dual(const smla_args* a, const smla_extra_args* x, int32_t num_splits, void* workspace,
                            size_t workspace_bytes, smla_stream_t stream) {
   g_last_error[0] = 0;
+  Range range("sparse_mla_decode_dual");
   int rc = validate(a);
   if (rc != SMLA_OK) return rc;
   if ((rc = validate_extra(a, x)) != SMLA_OK) return rc;
@@ -370,6 +434,7 @@ int sparse_mla_decode_dual(const smla_args* a, const smla_extra_args* x, int32_t
 
 int sparse_mla_resolve_rows(const smla_args* a, int32_t* rows_out, int64_t rows_stride_t, smla_stream_t stream) {
   g_last_error[0] = 0;
+  Range range("sparse_mla_resolve_rows");
   int rc = validate(a);
   if (rc != SMLA_OK) return rc;
   if (a->T == 0) return SMLA_OK;
@@ -386,6 +451,7 @@ int sparse_mla_resolve_rows(const smla_args* a, int32_t* rows_out, int64_t rows_
 int sparse_mla_resolve_rows_dual(const smla_args* a, const smla_extra_args* x, int32_t* rows_out,
                                  int64_t rows_stride_t, smla_stream_t stream) {
   g_last_error[0] = 0;
+  Range range("sparse_mla_resolve_rows_dual");
   int rc = validate(a);
   if (rc != SMLA_OK) return rc;
   if ((rc = validate_extra(a, x)) != SMLA_OK) return rc;
@@ -430,10 +496,12 @@ int validate_args(const smla_args* a) { return validate(a); }
 int setup_device(int* dev) { return device_setup(dev); }
 KParams params_for(const smla_args* a, int dev) { return make_params(a, dev); }
 int num_sms(int dev) { return g_num_sms[dev]; }
-int decode_splits(int T, int H, int topk, int num_splits, int sms) {
-  return splits_for(T, H, topk, num_splits, sms);
+int64_t l2_bytes(int dev) { return g_l2_bytes[dev]; }
+int decode_splits(int T, int H, int topk, int num_splits, int sms, int64_t l2_bytes) {
+  return splits_for(T, H, topk, num_splits, sms, l2_bytes);
 }
 size_t decode_ws_bytes(int64_t T, int64_t H, int64_t S) { return ws_bytes(T, H, S); }
 int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+void clear_error() { g_last_error[0] = 0; }
 }  // namespace host
 }  // namespace smla

@@ -21,9 +21,11 @@ int validate_args(const smla_args* a);
 int setup_device(int* dev);
 KParams params_for(const smla_args* a, int dev);
 int num_sms(int dev);
-int decode_splits(int T, int H, int topk, int num_splits, int sms);
+int64_t l2_bytes(int dev);
+int decode_splits(int T, int H, int topk, int num_splits, int sms, int64_t l2_bytes);
 size_t decode_ws_bytes(int64_t T, int64_t H, int64_t S);
 int set_error(int code, const char* msg);
+void clear_error();
 }  // namespace host
 }  // namespace smla
 
@@ -59,7 +61,10 @@ int scratch_address(int dev, void** out) {
 
 }  // namespace
 
+extern "C" size_t sparse_mla_noalloc_scratch_bytes(void) { return sizeof(g_noalloc_scratch); }
+
 extern "C" int sparse_mla_decode_noalloc(const smla_args* a, int32_t num_splits, smla_stream_t stream) {
+  smla::host::clear_error();
   int rc = smla::host::validate_args(a);
   if (rc != SMLA_OK) return rc;
   if (num_splits < 0 || num_splits > SMLA_MAX_SPLITS)
@@ -68,7 +73,14 @@ extern "C" int sparse_mla_decode_noalloc(const smla_args* a, int32_t num_splits,
   int dev = 0;
   if ((rc = smla::host::setup_device(&dev)) != SMLA_OK) return rc;
   if (dev >= kMaxDev) return smla::host::set_error(SMLA_ERR_UNSUPPORTED, "device ordinal above 63");
-  const int S = smla::host::decode_splits(a->T, a->H, a->topk, num_splits, smla::host::num_sms(dev));
+  int S = smla::host::decode_splits(a->T, a->H, a->topk, num_splits, smla::host::num_sms(dev),
+                                    smla::host::l2_bytes(dev));
+  if (num_splits == 0) {
+    // automatic choice: the largest split count up to the model's pick whose
+    // partials fit the array (one split needs none, so some count always fits)
+    while (S > 1 && smla::host::decode_ws_bytes(a->T, a->H, S) > sizeof(g_noalloc_scratch))
+      S = smla::host::decode_splits(a->T, a->H, a->topk, S - 1, 0, 0);
+  }
   smla::KParams p = smla::host::params_for(a, dev);
   const int chunks = (a->topk + 63) / 64;
   p.num_splits = S;

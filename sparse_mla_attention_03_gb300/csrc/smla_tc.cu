@@ -39,9 +39,10 @@
 //   warps 12-15 with warps 8-11: the load and conversion of q before the first
 //               tile, and half of the epilogue's stores after the last.
 //
-// Every mbarrier wait is bounded (about one second of global time); on timeout
-// the CTA sets the error word, stops, drains its issued MMAs, frees TMEM and
-// returns without writing outputs.
+// Every mbarrier wait is bounded (KParams::wait_ns of global time, one second
+// unless the caller set another limit); when a limit runs out the CTA sets the
+// error word, stops, drains its issued MMAs, frees TMEM and returns without
+// writing outputs.
 #include "smla_common.cuh"
 #include "smla_launch.h"
 
@@ -53,7 +54,9 @@ constexpr int HG = 64;   // heads per CTA (MMA N)
 constexpr int NT = 512;   // 8 producer warps, 4 softmax warps, 1 MMA warp, 3 helpers (q, epilogue)
 constexpr int W_SOFT = 8;
 constexpr int W_MMA = 12;
-constexpr uint64_t kTimeoutNs = 1000000000ull;
+// Limit of the final wait for already-issued MMAs (they always complete; the
+// call's own wait limit, which may be set as low as zero, does not apply).
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int OFF_TILE = 0;                       // 8 x 16384
@@ -95,15 +98,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait.  Returns false if the CTA is aborting (timeout here or elsewhere).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+// Non-blocking test of a phase (mbarrier.try_wait may suspend the thread for a
+// while before it reports an incomplete phase; test_wait never does).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (limit: KParams::wait_ns).  Returns false if the CTA is
+// aborting (the limit ran out here or in another role).  A zero limit gives
+// up at once unless the phase is already complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, const KParams& p) {
+  int* err = p.err;
+  if (p.wait_ns == 0) {
+    if (mbar_test_wait(bar, parity)) return true;
+    atomicOr(err, kErrTimeout);
+    *abort_flag = 1;
+    return false;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
+      if (globaltimer() - t0 > p.wait_ns) {
         atomicOr(err, kErrTimeout);
         *abort_flag = 1;
         return false;
@@ -119,8 +142,9 @@ __device__ __forceinline__ float ex2(float x) {
 // Warp-uniform bounded wait: every lane polls (a lane-0-only poll leaves the
 // warp diverged, and MMAs issued by a diverged warp run several times
 // slower), and the warp agrees on the verdict.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, err);
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               const KParams& p) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, p);
   return __all_sync(0xffffffffu, ok);
 }
 __device__ __forceinline__ void fence_proxy_async() {
@@ -501,7 +525,8 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
 #pragma unroll
     for (int g = 0; g < 5; ++g) {
       // this region of the tile is free once the previous tile's PV used it
-      if (it > 0 && !mbar_wait(bars + 8u * (B_PV0 + (g < 4 ? g : 3)), (it - 1) & 1, s_abort, p.err)) return;
+      // (warp-uniform: the warp leaves together, its shuffles stay converged)
+      if (it > 0 && !mbar_wait_warp(bars + 8u * (B_PV0 + (g < 4 ? g : 3)), (it - 1) & 1, s_abort, p)) return;
       if (g < 4) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -841,7 +866,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       auto issue_st = [&](int it) -> bool {
 #pragma unroll 1
         for (int g = 0; g < 4; ++g) {
-          if (!mbar_wait_warp(bar(B_KV0 + g), it & 1, s_abort, p.err)) return false;
+          if (!mbar_wait_warp(bar(B_KV0 + g), it & 1, s_abort, p)) return false;
           tc_fence_after();
           uint32_t ag = ad_tile + (uint32_t)g * (2 * 16384 >> 4), bg = bd_q + (uint32_t)g * (2 * 8192 >> 4);
           asm volatile("" : "+r"(ag), "+r"(bg));  // keep the group's bases in registers, not its 16 operands
@@ -855,7 +880,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
         // the rope group is waited for even without rope (p.nope: its bytes are
         // padding and its MMAs are skipped), so that the tile region where P^T
         // will be written is no longer being stored to
-        if (!mbar_wait_warp(bar(B_KV0 + 4), it & 1, s_abort, p.err)) return false;
+        if (!mbar_wait_warp(bar(B_KV0 + 4), it & 1, s_abort, p)) return false;
         tc_fence_after();
         if (!p.nope) {
 #pragma unroll
@@ -868,7 +893,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       };
       // O^T += V_tile^T . P^T, one commit per 128-row d_v chunk
       auto issue_pv = [&](int it) -> bool {
-        if (!mbar_wait_warp(bar(B_PFULL), it & 1, s_abort, p.err)) return false;
+        if (!mbar_wait_warp(bar(B_PFULL), it & 1, s_abort, p)) return false;
         tc_fence_after();
         const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll 1
@@ -882,7 +907,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
         }
         return true;
       };
-      const bool q_ok = ntiles == 0 || mbar_wait_warp(bar(B_QCONV), 0, s_abort, p.err);
+      const bool q_ok = ntiles == 0 || mbar_wait_warp(bar(B_QCONV), 0, s_abort, p);
       for (int it = 0; it < ntiles && q_ok; ++it) {
         if (!issue_st(it)) break;
         if (!issue_pv(it)) break;
@@ -891,7 +916,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       mma_commit(bar(B_DRAIN));
       const uint64_t t0 = globaltimer();
       while (!mbar_try_wait(bar(B_DRAIN), 0)) {
-        if (globaltimer() - t0 > kTimeoutNs) {
+        if (globaltimer() - t0 > kDrainLimitNs) {
           if (lane == 0) atomicOr(p.err, kErrTimeout);
           break;
         }
@@ -938,7 +963,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       const int idx1 = idx_ahead;
       const int slot2 = slot + 2 * BM;
       idx_ahead = it + 2 < ntiles ? index_at(slot2) : -1;
-      const bool failed = !mbar_wait(bar(B_SFULL), it & 1, s_abort, p.err);
+      const bool failed = !mbar_wait(bar(B_SFULL), it & 1, s_abort, p);
       if (bar_or(1, 128, failed)) {
         alive = false;
         break;
@@ -1042,7 +1067,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     }
     // ---------------------------------------------------------- epilogue
     bool failed = !alive;
-    if (alive && ntiles > 0 && !mbar_wait(bar(B_PV0 + 3), (ntiles - 1) & 1, s_abort, p.err)) failed = true;
+    if (alive && ntiles > 0 && !mbar_wait(bar(B_PV0 + 3), (ntiles - 1) & 1, s_abort, p)) failed = true;
     s_lsum[q4 * 64 + lane] = lsum0;
     s_lsum[q4 * 64 + 32 + lane] = lsum1;
     alive = !bar_or(1, 128, failed);

@@ -63,8 +63,15 @@ def assert_close(out_gpu, lse_gpu, out_ref, lse_ref, tag=""):
     return float(err.max()), float(err.mean())
 
 
-def sample_tokens(T, n, seed=0, must=()):
+def sample_tokens_by_quarter(T, n, seed=0, must=()):
+    """A seeded sample of about ``n`` distinct tokens of ``range(T)``: n/4 from
+    each quarter of the range (all of them when T <= n), plus ``must``."""
+    if T <= n:
+        return np.arange(T)
     rng = np.random.default_rng(seed)
     pick = set(int(x) for x in must if 0 <= x < T)
-    pick.update(int(x) for x in rng.choice(T, size=min(n, T), replace=False))
+    bounds = [q * T // 4 for q in range(5)]
+    for q in range(4):
+        lo, hi = bounds[q], bounds[q + 1]
+        pick.update(int(x) for x in lo + rng.choice(hi - lo, size=min(n // 4, hi - lo), replace=False))
     return np.array(sorted(pick))

@@ -114,7 +114,66 @@ def test_explicit_split_arithmetic(lib):
     assert lib.sparse_mla_decode_num_splits(4, 8, 640, 3) == 3
     ws = lib.sparse_mla_decode_workspace_size(128, 64, 2048, 8)
     assert ws == 128 * 64 * 8 * 512 * 4 + 128 * 64 * 8 * 4
-    assert lib.sparse_mla_abi_version() == 4
+    assert lib.sparse_mla_abi_version() == 5
+
+
+# Split choice for a described device (host only).  The wave model alone picks
+# these counts at 152 SMs (they match measured split sweeps on GB300); the
+# L2-footprint guard only acts when a token's rows are gathered by more than
+# one CTA (H=128 on the tcgen05 kernel, H=24 on the 8-head warp-MMA kernel).
+L2_GB300 = 126_500_000
+
+
+@pytest.mark.parametrize("T,H,topk,want", [
+    (8, 64, 2048, 16), (32, 64, 2048, 4), (64, 64, 2048, 2), (128, 64, 2048, 1), (256, 64, 2048, 1),
+    (32, 128, 2048, 2), (16, 64, 8192, 8), (64, 64, 512, 2), (8, 8, 4096, 32), (32, 8, 2048, 16),
+    (128, 8, 2048, 4), (512, 8, 1024, 1), (64, 16, 2048, 4), (16, 24, 2048, 8), (256, 8, 640, 2),
+])
+def test_wave_model_picks(lib, T, H, topk, want):
+    assert lib.sparse_mla_plan_num_splits(T, H, topk, 0, 152, L2_GB300) == want
+    assert lib.sparse_mla_plan_num_splits(T, H, topk, 0, 152, 0) == want  # no L2 figure: guard off
+
+
+def test_l2_footprint_guard():
+    lib = binding.load()
+    plan = lambda T, H, topk, l2: lib.sparse_mla_plan_num_splits(T, H, topk, 0, 152, l2)
+    chunk = 64 * 656
+    # one CTA per token (H=64): no row is read twice, the guard never acts
+    assert plan(128, 64, 3200, L2_GB300) == plan(128, 64, 3200, 10 ** 15) == 1
+    assert plan(128, 64, 3200, 1) == 1
+    # H=128, T=64, topk 2048: the two head-group CTAs of a token read its rows
+    # side by side (span 2 at one split): 2 x 32 chunks of rows, far inside
+    # GB300's L2, so the wave model's pick (one split) stands
+    assert plan(64, 128, 2048, L2_GB300) == plan(64, 128, 2048, 10 ** 15) == 1
+    # with an L2 smaller than that footprint the guard moves to the cheapest
+    # count that fits: S=2 streams 3 CTAs x 16 chunks between the reads
+    assert 2 * 32 * chunk > 3 * 16 * chunk
+    assert plan(64, 128, 2048, 3 * 16 * chunk) == 2
+    assert plan(64, 128, 2048, 5 * 8 * chunk) == 4
+    # and falls back to the unconstrained pick when nothing fits
+    assert plan(64, 128, 2048, 1) == 1
+    # an explicit count is never changed by the guard
+    assert lib.sparse_mla_plan_num_splits(64, 128, 2048, 1, 152, 1) == 1
+    # invalid descriptions
+    assert lib.sparse_mla_plan_num_splits(64, 128, 2048, 0, 0, L2_GB300) == 0
+    assert lib.sparse_mla_plan_num_splits(64, 128, 2048, 0, 152, -1) == 0
+
+
+def test_noalloc_scratch_size_matches_header(lib):
+    src = open(os.path.join(ROOT, "include", "sparse_mla.h")).read()
+    m = re.search(r"#define SMLA_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", src)
+    assert m
+    assert binding.noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+
+
+def test_wait_limit_setter_round_trips(lib):
+    prev = binding.set_wait_limit_ns(12345)
+    try:
+        assert prev == 1_000_000_000
+        assert binding.set_wait_limit_ns(0) == 12345
+    finally:
+        binding.set_wait_limit_ns(prev)
+    assert binding.set_wait_limit_ns(prev) == prev
 
 
 # ----------------------------------------------------------------------------- bench helpers (host logic)

@@ -10,7 +10,7 @@ import torch
 
 import oracle.sparse_mla_oracle as O
 from sparse_mla_attention_03_gb300 import binding, inputs
-from tests.helpers import assert_close, oracle_dual_for, oracle_for, sample_tokens, to_dev
+from tests.helpers import assert_close, oracle_dual_for, oracle_for, sample_tokens_by_quarter, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -205,6 +205,48 @@ def test_deterministic_repeat():
     a = run_prefill(wl)
     b = run_prefill(wl)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# ----------------------------------------------------------------------------- bounded waits
+@pytest.mark.parametrize("mode", ["prefill", "decode_split3"])
+def test_wait_limit_runs_out_and_the_context_stays_usable(mode):
+    # A zero wait limit makes the first mbarrier wait of the tcgen05 kernel that
+    # does not succeed at once give up: the call ends with SMLA_ERRF_TIMEOUT in
+    # the error word instead of hanging, and the next call on the same stream,
+    # with the default limit, is correct.
+    wl = inputs.make_prefill("waitlim", T=2, H=64, ctx=2048, topk=512, seed=311)
+    call = run_prefill if mode == "prefill" else (lambda w: run_decode(w, num_splits=3))
+    prev = binding.set_wait_limit_ns(0)
+    try:
+        call(wl)
+        flags = binding.get_error_word()
+    finally:
+        binding.set_wait_limit_ns(prev)
+    assert flags & binding.ERRF_TIMEOUT
+    out, lse = call(wl)
+    assert_close(out, lse, *oracle_for(wl), tag=f"{mode} after a timed-out call")
+    assert binding.get_error_word() == 0
+
+
+# ----------------------------------------------------------------------------- split choice, L2 guard
+def test_decode_split_choice_beyond_l2_and_guard_limited_count():
+    # H=128, 64 tokens, topk 2048, a 344 MB paged cache: the rows of each token
+    # are gathered by two CTAs (two head groups).  The automatic choice is the
+    # planner's for this device; on an L2 too small for those CTAs' rows the
+    # L2-footprint guard would take more splits.  Both counts are correct.
+    wl = inputs.make_decode("guard", n_req=32, tokens_per_req=2, H=128, ctx_per_req=16384, topk=2048, seed=321)
+    props = torch.cuda.get_device_properties(0)
+    sms, l2 = props.multi_processor_count, props.L2_cache_size
+    auto = binding.decode_num_splits(wl.T, wl.H, wl.topk)
+    assert auto == binding.plan_num_splits(wl.T, wl.H, wl.topk, 0, sms, l2)
+    small_l2 = 3 * 16 * 64 * 656  # fits two splits' streamed rows, not one split's
+    guarded = binding.plan_num_splits(wl.T, wl.H, wl.topk, 0, sms, small_l2)
+    assert guarded > binding.plan_num_splits(wl.T, wl.H, wl.topk, 0, sms, 10 ** 15)
+    ref = oracle_for(wl)
+    for s_ in sorted({0, guarded}):
+        out, lse = run_decode(wl, num_splits=s_)
+        assert_close(out, lse, *ref, tag=f"beyond-L2 H=128 decode S={s_ or auto}")
+    assert binding.get_error_word() == 0
 
 
 # ----------------------------------------------------------------------------- caches beyond L2
@@ -424,28 +466,37 @@ def test_arbitrary_scales(H):
 
 
 # ----------------------------------------------------------------------------- full-size workloads
+# Each full-size workload runs in the benchmark's launch configuration (the
+# automatic split count for decode); the oracle then checks a seeded sample of
+# at least 256 query tokens, drawn evenly from the four quarters of the token
+# range so that CTAs of every wave are covered, plus the first and last token.
+# Workloads with fewer tokens than that are checked on every token.
 FULL = {
-    "prefill16k_k512": (lambda: inputs.prefill_16k(512), "prefill", 48),
-    "prefill16k_k1024": (lambda: inputs.prefill_16k(1024), "prefill", 48),
-    "fewhead": (inputs.fewhead_prefill, "prefill", 96),
-    "decode": (inputs.batched_decode, "decode", 48),
-    "large": (inputs.large_prefill, "prefill", 24),
-    "dual_decode": (inputs.dual_decode, "dual_decode", 32),
-    "prefill16k_int8_k1024": (inputs.prefill_16k_int8, "prefill", 32),
+    "prefill16k_k512": (lambda: inputs.prefill_16k(512), "prefill"),
+    "prefill16k_k1024": (lambda: inputs.prefill_16k(1024), "prefill"),
+    "fewhead": (inputs.fewhead_prefill, "prefill"),
+    "decode": (inputs.batched_decode, "decode"),
+    "large": (inputs.large_prefill, "prefill"),
+    "dual_decode": (inputs.dual_decode, "dual_decode"),
+    "prefill16k_int8_k1024": (inputs.prefill_16k_int8, "prefill"),
 }
+FULL_SAMPLE = 256
 
 
 @pytest.mark.parametrize("name", list(FULL))
 def test_full_size_workload_sampled(name):
-    make, kind, n = FULL[name]
+    make, kind = FULL[name]
     wl = make()
     if kind == "dual_decode":
         out, lse = run_dual(wl, decode=True)
     else:
         out, lse = (run_prefill(wl) if kind == "prefill" else run_decode(wl))
-    toks = sample_tokens(wl.T, n, seed=5, must=(0, wl.T - 1))
+    toks = sample_tokens_by_quarter(wl.T, FULL_SAMPLE, seed=5, must=(0, wl.T - 1))
+    assert len(toks) >= min(FULL_SAMPLE, wl.T)
+    for q in range(4):  # every quarter of the token range is represented
+        assert np.any((toks >= q * wl.T // 4) & (toks < (q + 1) * wl.T // 4))
     ref = oracle_dual_for(wl, tokens=toks) if wl.dual else oracle_for(wl, tokens=toks)
     tt = torch.as_tensor(toks, device=out.device)
-    assert_close(out[tt], lse[tt], *ref, tag=name)
+    assert_close(out[tt], lse[tt], *ref, tag=f"{name} ({len(toks)} of {wl.T} tokens)")
     assert torch.isfinite(out).all()
     assert binding.get_error_word() == 0

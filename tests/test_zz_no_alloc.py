@@ -49,7 +49,7 @@ def test_noalloc_single_split_needs_no_scratch(cuda_lib):
     # one split writes the outputs directly: a size whose partials would not
     # fit the built-in array still runs, and matches the workspace decode
     wl = inputs.make_prefill("noalloc_s1", T=512, H=64, ctx=2048, topk=2048, seed=10)
-    assert binding.decode_workspace_size(wl.T, wl.H, wl.topk, 1) > binding.NOALLOC_SCRATCH_BYTES
+    assert binding.decode_workspace_size(wl.T, wl.H, wl.topk, 1) > binding.noalloc_scratch_bytes()
     ref, got = _both(wl, 1)
     assert torch.equal(ref[0], got[0]) and torch.equal(ref[1], got[1])
 
@@ -57,9 +57,22 @@ def test_noalloc_single_split_needs_no_scratch(cuda_lib):
 def test_noalloc_rejects_requests_beyond_the_array(cuda_lib):
     wl = inputs.make_prefill("noalloc_big", T=512, H=64, ctx=2048, topk=2048, seed=9, sink=None)
     need = binding.decode_workspace_size(wl.T, wl.H, wl.topk, 8)
-    assert need > binding.NOALLOC_SCRATCH_BYTES
+    assert need > binding.noalloc_scratch_bytes()
     d = _dev(wl)
     with pytest.raises(binding.SparseMLAError) as ei:
         binding.sparse_mla_decode_noalloc(d["q"], d["kv"], d["indices"], wl.sm_scale, num_splits=8)
     assert ei.value.code == binding.SMLA_ERR_INVALID
     assert "scratch" in str(ei.value)
+
+
+def test_noalloc_automatic_split_count(cuda_lib):
+    # num_splits = 0: the automatic choice (here more than one split, so the
+    # partials go through the built-in array) -- lowered to fit the array if
+    # it ever needed more; on 152 SMs the automatic choice stays well within it
+    wl = inputs.make_decode("noalloc_auto", n_req=16, tokens_per_req=2, H=128, ctx_per_req=8192, topk=2048, seed=11)
+    s = binding.decode_num_splits(wl.T, wl.H, wl.topk, 0)
+    assert s > 1 and binding.decode_workspace_size(wl.T, wl.H, wl.topk, 0) <= binding.noalloc_scratch_bytes()
+    for _ in range(2):
+        ref, got = _both(wl, 0)
+        assert_close(got[0], got[1], ref[0].double().cpu().numpy(), ref[1].double().cpu().numpy(),
+                     tag="noalloc automatic splits")
