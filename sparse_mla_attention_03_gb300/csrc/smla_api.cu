@@ -143,7 +143,6 @@ smla::KParams make_params(const smla_args* a, int dev) {
   p.big_cache = (int64_t)a->num_pages * SMLA_PAGE * SMLA_ROW_BYTES > g_l2_bytes[dev] / 4 ? 1 : 0;
   p.err = g_err_ptr[dev];
   p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
-  p.cta_slots = g_num_sms[dev];
   p.kv_format = a->kv_format;
   p.nope = a->layout == SMLA_LAYOUT_NOPE ? 1 : 0;
   // one list: the second-list fields stay inert

@@ -82,8 +82,6 @@ struct KParams {
   const int32_t* topk_length2;  // nullptr: topk2
   int* err;           // device error word
   uint64_t wait_ns;   // limit of each bounded in-kernel wait (GPU global time)
-  int32_t cta_slots;  // CTAs of the tcgen05 kernel resident at once (one per SM)
-  int32_t pad2_;
 };
 
 // ---------------------------------------------------------------------------

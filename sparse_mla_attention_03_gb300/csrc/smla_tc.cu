@@ -586,7 +586,10 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
 
 // Epilogue: parts [part_lo, part_hi) of the 8 (d_v chunk, 32-head half)
 // parts of O^T, by a warp whose TMEM lane quarter is q4.  s_alpha holds
-// the per-head normaliser.
+// the per-head normaliser.  kStream: final out is written with the
+// evict-first (streaming) cache operator, so that it does not push gathered
+// rows of a cache larger than L2 out of L2 (the HBM-resident load policy).
+template <bool kStream>
 __device__ __forceinline__ void store_parts(const KParams& p, const float* s_alpha, uint32_t T_O,
                                             uint32_t lane_off, int t, int h0, int split, int ntiles, int q4,
                                             int lane, int part_lo, int part_hi) {
@@ -638,7 +641,10 @@ __device__ __forceinline__ void store_parts(const KParams& p, const float* s_alp
         const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
         const uint2 st = hi2 ? make_uint2(recv, keep) : make_uint2(keep, recv);
         if (out_al8) {
-          *reinterpret_cast<uint2*>(ob + (int64_t)j * kDV) = st;
+          if (kStream)
+            __stcs(reinterpret_cast<uint2*>(ob + (int64_t)j * kDV), st);
+          else
+            *reinterpret_cast<uint2*>(ob + (int64_t)j * kDV) = st;
         } else {
           unsigned short* os = reinterpret_cast<unsigned short*>(ob + (int64_t)j * kDV);
           os[0] = (unsigned short)(st.x & 0xFFFFu);
@@ -683,6 +689,10 @@ __device__ __forceinline__ void store_parts(const KParams& p, const float* s_alp
 // the exponent of that maximum is the largest exponent field of the head's
 // bf16 values (an integer max over 16-bit halves), except when it is 0 or 255
 // (all zero or subnormal; Inf/NaN), where the float maximum decides.
+// kStream: q is read with the evict-first (streaming) cache operator (it is
+// read once), for the HBM-resident load policy, whose cached rows should keep
+// their L2 lines; otherwise it is copied with cp.async.
+template <bool kStream>
 __device__ __forceinline__ void load_q(const KParams& p, uint8_t* smem, uint32_t sbase, int t, int h0, int qc,
                                        float* s_qmul, float* s_mref, float* s_mneg, uint32_t bars) {
   const __nv_bfloat16* qsrc = p.q + (int64_t)t * p.q_stride_t + (int64_t)h0 * (p.nope ? kDNope : kDQK);
@@ -705,10 +715,16 @@ __device__ __forceinline__ void load_q(const KParams& p, uint8_t* smem, uint32_t
       }
     }
   } else if ((reinterpret_cast<uintptr_t>(qsrc) & 15) == 0) {
+    if (kStream) {
+      const uint4* qv = reinterpret_cast<const uint4*>(qsrc);
+#pragma unroll 6
+      for (int f = qc; f < HG * 72; f += 256) sts128(sbase + q_chunk_off(f / 72, f % 72), __ldcs(qv + f));
+    } else {
 #pragma unroll 2
-    for (int f = qc; f < HG * 72; f += 256) cp_async16(sbase + q_chunk_off(f / 72, f % 72), qsrc + 8 * f, 16);
-    cp_async_commit();
-    cp_async_wait<0>();
+      for (int f = qc; f < HG * 72; f += 256) cp_async16(sbase + q_chunk_off(f / 72, f % 72), qsrc + 8 * f, 16);
+      cp_async_commit();
+      cp_async_wait<0>();
+    }
   } else {
     const unsigned short* qs = reinterpret_cast<const unsigned short*>(qsrc);
 #pragma unroll 2
@@ -851,7 +867,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   } else if (warp >= W_MMA) {
     // ============================================ q conversion, MMA issue (warp 12), epilogue
     asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
-    load_q(p, smem, sbase, t, h0, tid - 256, reinterpret_cast<float*>(smem + OFF_QMUL),
+    load_q<kEarly>(p, smem, sbase, t, h0, tid - 256, reinterpret_cast<float*>(smem + OFF_QMUL),
            reinterpret_cast<float*>(smem + OFF_MREF), reinterpret_cast<float*>(smem + OFF_MNEG), bars);
     if (warp == W_MMA) {
       const uint32_t id_f16 = idesc(0, 0, 0);
@@ -928,7 +944,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     named_bar(2, 256);
     if (*s_epi) {
       tc_fence_after();
-      store_parts(p, s_alpha, T_O, (uint32_t)((warp & 3) * 32) << 16, t, h0, split, ntiles, warp & 3, lane, 4, 8);
+      store_parts<kEarly>(p, s_alpha, T_O, (uint32_t)((warp & 3) * 32) << 16, t, h0, split, ntiles, warp & 3, lane, 4, 8);
     }
   } else {
     // ============================================================ softmax + epilogue
@@ -940,7 +956,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     // read now so that the load is long done by the epilogue
     const float sink_lo = (q4 == 0 && p.attn_sink) ? __ldg(p.attn_sink + h0 + lane) : 0.f;
     const float sink_hi = (q4 == 0 && p.attn_sink) ? __ldg(p.attn_sink + h0 + lane + 32) : 0.f;
-    load_q(p, smem, sbase, t, h0, c, s_qmul, s_mref, s_mneg, bars);
+    load_q<kEarly>(p, smem, sbase, t, h0, c, s_qmul, s_mref, s_mneg, bars);
 
     // running sums of P per head: lane l keeps heads l and l+32 of this warp's
     // 32 candidates (summed over the warp by a transpose-reduction per tile)
@@ -1103,7 +1119,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     // are published to it by the barrier below
     if (warp == W_SOFT && lane == 0) *s_epi = alive ? 1 : 0;
     named_bar(2, 256);
-    if (alive) store_parts(p, s_alpha, T_O, lane_off, t, h0, split, ntiles, q4, lane, 0, 4);
+    if (alive) store_parts<kEarly>(p, s_alpha, T_O, lane_off, t, h0, split, ntiles, q4, lane, 0, 4);
   }
   tc_fence_before();
   __syncthreads();
