@@ -255,11 +255,20 @@ int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags);
  * spun forever on mbarrier_wait_parity).  When a limit runs out, the CTA sets
  * SMLA_ERRF_TIMEOUT, stops every role, waits for its issued MMAs, frees its
  * tensor memory and returns without writing its outputs; the context stays
- * usable.  A limit of 0 makes the first wait that does not succeed at once
- * give up: a test hook for that path.  The limit in force is read when a call
- * is made; calls already queued keep theirs.
+ * usable.  The limit in force is read when a call is made; calls already
+ * queued keep theirs.
  */
 uint64_t sparse_mla_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test hook for the path above: while on (non-zero), the producers of the
+ * tcgen05 kernel (H % 64 == 0) gather nothing in the calls made after it, on
+ * any thread, so the MMA issue's first wait is never completed and runs out
+ * after the wait limit; the call ends with SMLA_ERRF_TIMEOUT and unwritten
+ * outputs.  Off by default; returns the previous setting.  Not for use
+ * outside tests.
+ */
+int32_t sparse_mla_set_test_stall(int32_t on);
 
 /*
  * Decode without any device allocation -- no counterpart on the pages; added

@@ -74,6 +74,7 @@ SYMBOLS = {
     "sparse_mla_decode_noalloc": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_void_p]),
     "sparse_mla_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "sparse_mla_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+    "sparse_mla_set_test_stall": (ctypes.c_int32, [ctypes.c_int32]),
     "sparse_mla_get_error_word": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "sparse_mla_last_error": (ctypes.c_char_p, []),
     "sparse_mla_abi_version": (ctypes.c_int32, []),
@@ -251,6 +252,11 @@ def noalloc_scratch_bytes() -> int:
 def set_wait_limit_ns(ns: int) -> int:
     """Limit of every bounded in-kernel wait of later calls; returns the previous one."""
     return int(load().sparse_mla_set_wait_limit_ns(int(ns)))
+
+
+def set_test_stall(on: bool) -> bool:
+    """Test hook: the tcgen05 kernel's producers gather nothing (its waits run out); returns the previous setting."""
+    return bool(load().sparse_mla_set_test_stall(1 if on else 0))
 
 
 

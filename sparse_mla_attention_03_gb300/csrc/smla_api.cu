@@ -19,6 +19,7 @@ thread_local char g_last_error[512] = "";
 // Limit of every bounded in-kernel wait, for the calls that follow.
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int32_t> g_test_stall{0};
 
 // One NVTX range per entry point (named after it), for profiler timelines.
 struct Range {
@@ -143,6 +144,7 @@ smla::KParams make_params(const smla_args* a, int dev) {
   p.big_cache = (int64_t)a->num_pages * SMLA_PAGE * SMLA_ROW_BYTES > g_l2_bytes[dev] / 4 ? 1 : 0;
   p.err = g_err_ptr[dev];
   p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  p.test_stall = g_test_stall.load(std::memory_order_relaxed);
   p.kv_format = a->kv_format;
   p.nope = a->layout == SMLA_LAYOUT_NOPE ? 1 : 0;
   // one list: the second-list fields stay inert
@@ -336,6 +338,8 @@ extern "C" {
 int32_t sparse_mla_abi_version(void) { return 5; }
 
 uint64_t sparse_mla_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
+
+int32_t sparse_mla_set_test_stall(int32_t on) { return g_test_stall.exchange(on != 0 ? 1 : 0); }
 
 const char* sparse_mla_last_error(void) { return g_last_error; }
 

@@ -82,6 +82,8 @@ struct KParams {
   const int32_t* topk_length2;  // nullptr: topk2
   int* err;           // device error word
   uint64_t wait_ns;   // limit of each bounded in-kernel wait (GPU global time)
+  int32_t test_stall; // test hook: the tcgen05 kernel's producers gather nothing
+  int32_t pad2_;
 };
 
 // ---------------------------------------------------------------------------

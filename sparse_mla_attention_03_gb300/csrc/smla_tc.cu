@@ -98,28 +98,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Non-blocking test of a phase (mbarrier.try_wait may suspend the thread for a
-// while before it reports an incomplete phase; test_wait never does).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 // Bounded wait (limit: KParams::wait_ns).  Returns false if the CTA is
-// aborting (the limit ran out here or in another role).  A zero limit gives
-// up at once unless the phase is already complete.
+// aborting (the limit ran out here or in another role).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, const KParams& p) {
-  int* err = p.err;
-  if (p.wait_ns == 0) {
-    if (mbar_test_wait(bar, parity)) return true;
-    atomicOr(err, kErrTimeout);
-    *abort_flag = 1;
-    return false;
-  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
@@ -127,7 +108,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if ((i & 63u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer() - t0 > p.wait_ns) {
-        atomicOr(err, kErrTimeout);
+        atomicOr(p.err, kErrTimeout);
         *abort_flag = 1;
         return false;
       }
@@ -433,6 +414,9 @@ template <bool kEarly, bool kDual, bool kInt8>
 __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32_t sbase, uint32_t bars, int t,
                                          int len1, int lo, int hi, int ntiles, int pw, int lane,
                                          volatile int* s_abort) {
+  // test hook (sparse_mla_set_test_stall): no row is gathered, so the MMA
+  // issue's first wait runs out and the CTA takes its abort path
+  if (p.test_stall) return;
   const int32_t* btr = bt_row_of(p, t);
   const int32_t* btr2 = kDual ? bt2_row_of(p, t) : nullptr;
   float* s_sc = reinterpret_cast<float*>(smem + OFF_SCALE) + pw * 64;  // [16 rows][4]
@@ -525,8 +509,10 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
 #pragma unroll
     for (int g = 0; g < 5; ++g) {
       // this region of the tile is free once the previous tile's PV used it
-      // (warp-uniform: the warp leaves together, its shuffles stay converged)
-      if (it > 0 && !mbar_wait_warp(bars + 8u * (B_PV0 + (g < 4 ? g : 3)), (it - 1) & 1, s_abort, p)) return;
+      // (a per-lane wait: the lanes of the converged warp poll the barrier in
+      // the same instructions and see the same phase; a warp-wide agreement on
+      // every wait cost 1% of the 16k prefill)
+      if (it > 0 && !mbar_wait(bars + 8u * (B_PV0 + (g < 4 ? g : 3)), (it - 1) & 1, s_abort, p)) return;
       if (g < 4) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

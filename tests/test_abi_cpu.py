@@ -176,6 +176,15 @@ def test_wait_limit_setter_round_trips(lib):
     assert binding.set_wait_limit_ns(prev) == prev
 
 
+def test_test_stall_setter_round_trips(lib):
+    assert binding.set_test_stall(True) is False
+    try:
+        assert binding.set_test_stall(True) is True
+    finally:
+        binding.set_test_stall(False)
+    assert binding.set_test_stall(False) is False
+
+
 # ----------------------------------------------------------------------------- bench helpers (host logic)
 def test_bench_traffic_record_tracks_kernel_sources(tmp_path, monkeypatch):
     import json

@@ -210,17 +210,20 @@ def test_deterministic_repeat():
 # ----------------------------------------------------------------------------- bounded waits
 @pytest.mark.parametrize("mode", ["prefill", "decode_split3"])
 def test_wait_limit_runs_out_and_the_context_stays_usable(mode):
-    # A zero wait limit makes the first mbarrier wait of the tcgen05 kernel that
-    # does not succeed at once give up: the call ends with SMLA_ERRF_TIMEOUT in
-    # the error word instead of hanging, and the next call on the same stream,
-    # with the default limit, is correct.
+    # With the test hook on, the tcgen05 kernel's producers gather nothing, so
+    # the MMA issue's first wait is never completed.  With a 2 ms wait limit
+    # the call ends with SMLA_ERRF_TIMEOUT in the error word instead of
+    # hanging, and the next call on the same stream, hook off and default
+    # limit, is correct.
     wl = inputs.make_prefill("waitlim", T=2, H=64, ctx=2048, topk=512, seed=311)
     call = run_prefill if mode == "prefill" else (lambda w: run_decode(w, num_splits=3))
-    prev = binding.set_wait_limit_ns(0)
+    prev = binding.set_wait_limit_ns(2_000_000)
+    binding.set_test_stall(True)
     try:
         call(wl)
         flags = binding.get_error_word()
     finally:
+        binding.set_test_stall(False)
         binding.set_wait_limit_ns(prev)
     assert flags & binding.ERRF_TIMEOUT
     out, lse = call(wl)
