@@ -252,6 +252,21 @@ def test_decode_split_choice_beyond_l2_and_guard_limited_count():
     assert binding.get_error_word() == 0
 
 
+# ----------------------------------------------------------------------------- size limits
+@pytest.mark.parametrize("H,S", [(128, 0), (128, 64), (8, 64)])
+def test_maximum_heads_splits_and_topk(H, S):
+    # the largest head count, 64 splits (the maximum) and a 16384-slot index
+    # list (256 chunks of 64) over a paged 32768-position context, with a
+    # ragged topk_length so that some splits are empty
+    wl = inputs.make_decode("maxsize", n_req=2, tokens_per_req=2, H=H, ctx_per_req=32768, topk=16384, seed=331 + S)
+    wl.topk_length = torch.tensor([16384, 1, 9000, 0], dtype=torch.int32)
+    eff = binding.decode_num_splits(wl.T, wl.H, wl.topk, S)
+    assert S == 0 or eff == S
+    out, lse = run_decode(wl, num_splits=S)
+    assert_close(out, lse, *oracle_for(wl), tag=f"max H={H} S={S or eff} topk=16384")
+    assert binding.get_error_word() == 0
+
+
 # ----------------------------------------------------------------------------- caches beyond L2
 # A cache larger than a quarter of the device's L2 (at least 32 MB on GB300)
 # runs the tcgen05 kernel's early-load / L2-prefetch variant; these cases cover
