@@ -122,7 +122,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 // Warp-uniform bounded wait: every lane polls (a lane-0-only poll leaves the
 // warp diverged, and MMAs issued by a diverged warp run several times
-// slower), and the warp agrees on the verdict.
+// slower), and the warp agrees on the outcome.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                const KParams& p) {
   const bool ok = mbar_wait(bar, parity, abort_flag, p);

@@ -216,3 +216,19 @@ def test_bench_counts_valid_slots_of_both_lists():
     assert bench.valid_slots(wl) == want
     w = bench.work_of(wl)
     assert w["flops"] == 2.0 * 8 * (576 + 512) * want and w["gather_bytes"] == want * 656
+
+
+def test_bench_roofline_entries():
+    import bench
+    peaks = dict(hbm=6000.0, tflops=2000.0, tflops_sus=1800.0, src="measured")
+    work = dict(flops=2.0e12, bytes=3.0e9, valid=1)
+    # tensor-bound: algorithmic flops over the time, against the bf16 peak
+    r = bench.roofline_of("tensor", work, 2.0, peaks, "no-such-workload")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["achieved"] == 1000.0 and r["frac"] == 0.5 and r["traffic"] is None
+    # HBM-bound: algorithmic bytes over the time, labelled as such
+    r = bench.roofline_of("hbm", work, 1.0, peaks, "no-such-workload")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["achieved"] == 3000.0 and r["frac"] == 0.5
+    assert "algorithmic" in r["achieved_kind"]
+    # every workload timed beside the headline is a bench workload
+    assert set(bench.PER_CONFIG) <= set(bench.workloads())
