@@ -33,6 +33,7 @@ constexpr int TS = 704;   // shared row stride in bytes (44 x 16)
 constexpr int QS = 1168;  // shared q row stride in bytes (73 x 16)
 constexpr int PS = 160;   // shared P row stride in bytes (64 f16 + pad)
 constexpr int NT = 128;   // threads per CTA
+constexpr float kPScale = 256.f;  // power-of-two factor on the PV B operand (see the PV loop)
 
 // Bank-conflict swizzle of 16-byte chunks inside a staged row.  Chunks 0..39
 // are XOR-permuted by (row / 4) % 4 so that the transposing V reads of four
@@ -319,13 +320,20 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
       const float v1 = *reinterpret_cast<const float*>(r1 + swz(cb + 1, 32) * 16 + warp * 4);
       const float v2 = *reinterpret_cast<const float*>(r2 + swz(cb + 2, 32) * 16 + warp * 4);
       const float v3 = *reinterpret_cast<const float*>(r3 + swz(cb + 3, 32) * 16 + warp * 4);
-      const uint32_t sclo = pack_f16x2(v0, v1), schi = pack_f16x2(v2, v3);
+      const uint32_t sclo = pack_f16x2(v0 * kPScale, v1 * kPScale), schi = pack_f16x2(v2 * kPScale, v3 * kPScale);
+      // The row scales multiply P, not V: warp w's d_v columns are exactly
+      // scale block w, so candidate c's scale is one number for all of them,
+      // and P'[c][h] = P[c][h] * scale[c][w] * kPScale costs 2 multiplies per
+      // head group here instead of one per converted V pair.  kPScale (a
+      // power of two, removed in the epilogue) keeps P' in f16's normal range
+      // for small P (scale 2^-7, P down to about 2^-15) while the largest
+      // allowed scale (128) keeps it below 2^15.
       uint32_t bfr[NH8][2];
 #pragma unroll
       for (int n = 0; n < NH8; ++n) {
         const uint2 bv = *reinterpret_cast<const uint2*>(s_p + (n * 8 + g) * PS + (16 * kk + 4 * tq) * 2);
-        bfr[n][0] = bv.x;
-        bfr[n][1] = bv.y;
+        bfr[n][0] = hmul2_u32(bv.x, sclo);
+        bfr[n][1] = hmul2_u32(bv.y, schi);
       }
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) {
@@ -344,14 +352,6 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
         codes4_to_f16x2x2<kInt8>(x1, l1, h1_);
         codes4_to_f16x2x2<kInt8>(x2, l2, h2_);
         codes4_to_f16x2x2<kInt8>(x3, l3, h3_);
-        l0 = hmul2_u32(l0, sclo);
-        l1 = hmul2_u32(l1, sclo);
-        l2 = hmul2_u32(l2, sclo);
-        l3 = hmul2_u32(l3, sclo);
-        h0_ = hmul2_u32(h0_, schi);
-        h1_ = hmul2_u32(h1_, schi);
-        h2_ = hmul2_u32(h2_, schi);
-        h3_ = hmul2_u32(h3_, schi);
 #pragma unroll
         for (int n = 0; n < NH8; ++n) {
           mma_f16_16816(o[2 * pp][n], l0, l1, h0_, h1_, bfr[n][0], bfr[n][1]);
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
       if (final_out) {
         const float sk = p.attn_sink ? exp2f(__ldg(p.attn_sink + h) * kLog2e - muse) : 0.f;
         const float den = lt + sk;
-        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const float inv = den > 0.f ? 1.f / (den * kPScale) : 0.f;
         __nv_bfloat16* orow = p.out + (int64_t)t * p.out_stride_t + (int64_t)h * kDV;
 #pragma unroll
         for (int pp = 0; pp < 4; ++pp) {
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
         }
         if (warp == 0 && g == 0) p.lse[(int64_t)t * p.lse_stride_t + h] = lse_v;
       } else {
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const float inv = lt > 0.f ? 1.f / (lt * kPScale) : 0.f;
         const int64_t th = ((int64_t)t * p.H + h) * p.num_splits + split;
         float* wrow = p.ws_o + th * kDV;
 #pragma unroll
