@@ -489,22 +489,25 @@ def test_arbitrary_scales(H):
 # at least 256 query tokens, drawn evenly from the four quarters of the token
 # range so that CTAs of every wave are covered, plus the first and last token.
 # Workloads with fewer tokens than that are checked on every token.
-FULL = {
-    "prefill16k_k512": (lambda: inputs.prefill_16k(512), "prefill"),
-    "prefill16k_k1024": (lambda: inputs.prefill_16k(1024), "prefill"),
-    "fewhead": (inputs.fewhead_prefill, "prefill"),
-    "decode": (inputs.batched_decode, "decode"),
-    "large": (inputs.large_prefill, "prefill"),
-    "dual_decode": (inputs.dual_decode, "dual_decode"),
-    "prefill16k_int8_k1024": (inputs.prefill_16k_int8, "prefill"),
+FULL = {  # name: (generator, kind, query tokens)
+    "prefill16k_k512": (lambda: inputs.prefill_16k(512), "prefill", 1024),
+    "prefill16k_k1024": (lambda: inputs.prefill_16k(1024), "prefill", 1024),
+    "fewhead": (inputs.fewhead_prefill, "prefill", 8192),
+    "decode": (inputs.batched_decode, "decode", 128),
+    "large": (inputs.large_prefill, "prefill", 4096),
+    "dual_decode": (inputs.dual_decode, "dual_decode", 128),
+    "prefill16k_int8_k1024": (inputs.prefill_16k_int8, "prefill", 1024),
 }
 FULL_SAMPLE = 256
 
 
-@pytest.mark.parametrize("name", list(FULL))
+@pytest.mark.parametrize("name", list(FULL),
+                         ids=[f"{k}-{min(v[2], FULL_SAMPLE)}plus-of-{v[2]}-tokens" if v[2] > FULL_SAMPLE
+                              else f"{k}-all-{v[2]}-tokens" for k, v in FULL.items()])
 def test_full_size_workload_sampled(name):
-    make, kind = FULL[name]
+    make, kind, n_tokens = FULL[name]
     wl = make()
+    assert wl.T == n_tokens
     if kind == "dual_decode":
         out, lse = run_dual(wl, decode=True)
     else:
