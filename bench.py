@@ -400,11 +400,12 @@ def time_parts(parts, steps, warmup, flush, stream, barrier):
     return [[ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(steps)] for j in range(len(parts))]
 
 
-def roofline_of(bound, work, ms, peaks, workload):
-    """Roofline entry of one kernel launch set: algorithmic flops (tensor-bound
-    paths) or bytes (gather/HBM-bound paths) per launch over its measured time,
-    against the measured peak; `traffic` is the ncu DRAM bytes per launch when
-    a capture of the current kernel sources exists (and the DRAM rate it gives)."""
+def roofline_of(bound, work, ms, peaks, workload, launches=1):
+    """Roofline entry of the attention launches of one step (`launches` of
+    them in `ms`): algorithmic flops (tensor-bound paths) or bytes
+    (gather/HBM-bound paths) over the measured time, against the measured
+    peak; `traffic` is the ncu DRAM bytes per launch when a capture of the
+    current kernel sources exists, and `dram_gbs` the DRAM rate it gives."""
     sec = ms / 1e3
     if bound == "tensor":
         achieved = work["flops"] / sec / 1e12
@@ -421,8 +422,8 @@ def roofline_of(bound, work, ms, peaks, workload):
     if traffic is not None:
         r["traffic"] = traffic
         r["traffic_unit"] = "bytes per launch (mean), ncu dram__bytes_read.sum + dram__bytes_write.sum"
-        r["dram_gbs"] = round(traffic / sec / 1e9, 1)
-        r["dram_frac"] = round(traffic / sec / 1e9 / peaks["hbm"], 4)
+        r["dram_gbs"] = round(traffic * launches / sec / 1e9, 1)
+        r["dram_frac"] = round(traffic * launches / sec / 1e9 / peaks["hbm"], 4)
     if src is not None:
         r["traffic_source"] = src
     return r
@@ -447,7 +448,7 @@ def run_per_config(args, dev, stream, barrier, flush, peaks, l2_bytes):
         tokens = sum(p["wl"].T for p in parts)
         cache = sum(p["wl"].kv.numel() + (p["wl"].extra_kv.numel() if p["wl"].dual else 0) for p in parts)
         e = dict(workload=spec["name"], ms=round(ms, 4), query_tokens_per_s=round(tokens / (ms / 1e3), 1),
-                 roofline=roofline_of(spec["bound"], work, ms, peaks, key), cache_bytes=cache,
+                 roofline=roofline_of(spec["bound"], work, ms, peaks, key, launches=len(parts)), cache_bytes=cache,
                  cache_in_l2=bool(cache <= l2_bytes), gpu_launches_per_step=sum(p["launches"] for p in parts))
         if parts[0]["splits"] is not None:
             e["num_splits"] = parts[0]["splits"]
@@ -486,7 +487,7 @@ def run_ours(args, rank, world, local_rank):
 
     # roofline of the dominant kernel (the attention kernel; for decode the split kernel dominates)
     work = {k: sum(p["work"][k] for p in parts) for k in ("flops", "bytes", "valid")}
-    roof = roofline_of(spec["bound"], work, total_ms / args.steps, peaks, args.workload)
+    roof = roofline_of(spec["bound"], work, total_ms / args.steps, peaks, args.workload, launches=len(parts))
     roof["per_launch"] = {p["tag"]: dict(ms=round(statistics.mean(per_part_ms[j]), 4),
                                          tflops=round(p["work"]["flops"] / (statistics.mean(per_part_ms[j]) / 1e3) / 1e12, 2),
                                          gbs=round(p["work"]["bytes"] / (statistics.mean(per_part_ms[j]) / 1e3) / 1e9, 1))

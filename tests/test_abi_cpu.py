@@ -230,5 +230,12 @@ def test_bench_roofline_entries():
     r = bench.roofline_of("hbm", work, 1.0, peaks, "no-such-workload")
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["achieved"] == 3000.0 and r["frac"] == 0.5
     assert "algorithmic" in r["achieved_kind"]
+    # the DRAM rate counts every launch of the step
+    import json
+    rec_dir = os.path.join(str(bench.ROOT), "profiles")
+    traffic, _ = bench.dram_traffic("prefill16k")
+    if traffic is not None:
+        r2 = bench.roofline_of("tensor", work, 1.0, peaks, "prefill16k", launches=2)
+        assert r2["dram_gbs"] == round(traffic * 2 / 1e-3 / 1e9, 1)
     # every workload timed beside the headline is a bench workload
     assert set(bench.PER_CONFIG) <= set(bench.workloads())
