@@ -670,11 +670,12 @@ __device__ __forceinline__ void store_parts(const KParams& p, const float* s_alp
 // MMA-issue warp waits for q anyway; the other three have no other work).  The
 // 64 head rows (one contiguous 72 KB block, or 64 KB without rope) are copied
 // into their swizzled places in the q buffer, then converted in place: thread
-// qc handles head qc/4, chunks [18 (qc%4), 18 (qc%4) + 18) of its 72.  Each
-// head gets a power-of-two prescale putting its largest |q| in [2^14, 2^15);
-// the exponent of that maximum is the largest exponent field of the head's
-// bf16 values (an integer max over 16-bit halves), except when it is 0 or 255
-// (all zero or subnormal; Inf/NaN), where the float maximum decides.
+// qc handles head qc/4, chunks [18 (qc%4), 18 (qc%4) + 18) of its 72.  The
+// token gets one power-of-two prescale, putting the largest |q| of its 64
+// heads in [2^14, 2^15).  Each head's maximum exponent is the largest
+// exponent field of its bf16 values (an integer max over 16-bit halves),
+// except when that field is 0 or 255 (all zero or subnormal; Inf/NaN), where
+// the float maximum decides; the token takes the largest over its heads.
 // kStream: q is read with the evict-first (streaming) cache operator (it is
 // read once), for the HBM-resident load policy, whose cached rows should keep
 // their L2 lines; otherwise it is copied with cp.async.
@@ -739,6 +740,7 @@ __device__ __forceinline__ void load_q(const KParams& p, uint8_t* smem, uint32_t
   const int ef = (int)(m >> 7);  // largest exponent field of the head
   int e = ef - 141;              // the exponent of max|q| is ef - 126; prescale to [2^14, 2^15)
   e = e < -100 ? -100 : (e > 100 ? 100 : e);
+  bool e_valid = ef > 0 && ef < 255;  // the head has a finite, nonzero, normal maximum
   if (__any_sync(0xffffffffu, ef == 0 || ef == 255)) {
     float amax = 0.f;
 #pragma unroll 2
@@ -753,8 +755,28 @@ __device__ __forceinline__ void load_q(const KParams& p, uint8_t* smem, uint32_t
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    if (ef == 0 || ef == 255) e = q_prescale_exp(amax);
+    if (ef == 0 || ef == 255) {
+      e = q_prescale_exp(amax);
+      e_valid = amax > 0.f && isfinite(amax);
+    }
   }
+  // One prescale for the whole token: that of its largest head (heads with
+  // no finite nonzero value do not count).  Every head then shares one score
+  // factor, which the softmax keeps in a register instead of reading 64 of
+  // them from shared memory per tile.  A head's bf16 values stay exact in f16
+  // down to 2^-28 of the token's largest |q|; smaller ones only carry scores
+  // below that relative size.
+  int ev = e_valid ? e : -1000;
+  ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 4));
+  ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 8));
+  ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 16));
+  int* s_emax = reinterpret_cast<int*>(smem + OFF_TMAX);  // free until the softmax's first slow path
+  if ((qc & 31) == 0) s_emax[qc >> 5] = ev;
+  named_bar(2, 256);
+  ev = s_emax[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) ev = max(ev, s_emax[w]);
+  e = ev == -1000 ? 0 : ev;
   const float down = pow2f(-e);
 #pragma unroll 3
   for (int k = 0; k < 18; ++k) {
@@ -943,6 +965,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     const float sink_lo = (q4 == 0 && p.attn_sink) ? __ldg(p.attn_sink + h0 + lane) : 0.f;
     const float sink_hi = (q4 == 0 && p.attn_sink) ? __ldg(p.attn_sink + h0 + lane + 32) : 0.f;
     load_q<kEarly>(p, smem, sbase, t, h0, c, s_qmul, s_mref, s_mneg, bars);
+    const float qmul = s_qmul[0];  // the token's score factor (one q prescale for all heads)
 
     // running sums of P per head: lane l keeps heads l and l+32 of this warp's
     // 32 candidates (summed over the warp by a transpose-reduction per tile)
@@ -977,12 +1000,11 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       float dmax = -INFINITY;
 #pragma unroll
       for (int h4 = 0; h4 < 16; ++h4) {
-        const float4 qm = *reinterpret_cast<const float4*>(s_qmul + 4 * h4);
         const float4 mn = *reinterpret_cast<const float4*>(s_mneg + 4 * h4);
-        x[4 * h4 + 0] = fmaf(x[4 * h4 + 0], qm.x, mn.x);
-        x[4 * h4 + 1] = fmaf(x[4 * h4 + 1], qm.y, mn.y);
-        x[4 * h4 + 2] = fmaf(x[4 * h4 + 2], qm.z, mn.z);
-        x[4 * h4 + 3] = fmaf(x[4 * h4 + 3], qm.w, mn.w);
+        x[4 * h4 + 0] = fmaf(x[4 * h4 + 0], qmul, mn.x);
+        x[4 * h4 + 1] = fmaf(x[4 * h4 + 1], qmul, mn.y);
+        x[4 * h4 + 2] = fmaf(x[4 * h4 + 2], qmul, mn.z);
+        x[4 * h4 + 3] = fmaf(x[4 * h4 + 3], qmul, mn.w);
         dmax = fmaxf(dmax, fmaxf(fmaxf(x[4 * h4], x[4 * h4 + 1]), fmaxf(x[4 * h4 + 2], x[4 * h4 + 3])));
       }
       if (!valid) dmax = -INFINITY;
@@ -1036,12 +1058,11 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
         tmem_ld64(T_S + lane_off, x);
 #pragma unroll
         for (int h4 = 0; h4 < 16; ++h4) {
-          const float4 qm = *reinterpret_cast<const float4*>(s_qmul + 4 * h4);
           const float4 mn = *reinterpret_cast<const float4*>(s_mneg + 4 * h4);
-          x[4 * h4 + 0] = fmaf(x[4 * h4 + 0], qm.x, mn.x);
-          x[4 * h4 + 1] = fmaf(x[4 * h4 + 1], qm.y, mn.y);
-          x[4 * h4 + 2] = fmaf(x[4 * h4 + 2], qm.z, mn.z);
-          x[4 * h4 + 3] = fmaf(x[4 * h4 + 3], qm.w, mn.w);
+          x[4 * h4 + 0] = fmaf(x[4 * h4 + 0], qmul, mn.x);
+          x[4 * h4 + 1] = fmaf(x[4 * h4 + 1], qmul, mn.y);
+          x[4 * h4 + 2] = fmaf(x[4 * h4 + 2], qmul, mn.z);
+          x[4 * h4 + 3] = fmaf(x[4 * h4 + 3], qmul, mn.w);
         }
       }
       // P = exp2(x) rounded to f16 -> row c of P^T (MN-major: heads contiguous)

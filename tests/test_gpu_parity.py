@@ -291,7 +291,7 @@ def test_cache_beyond_l2_paged_decode(S):
 
 @pytest.mark.parametrize("H", [8, 64])
 def test_q_heads_zero_subnormal_and_large(H):
-    # the per-head q prescale: an all-zero head, a head of bf16 subnormals (the
+    # the q prescale: an all-zero head, a head of bf16 subnormals (the
     # exponent-field shortcut falls back to the float maximum) and large heads
     wl = inputs.make_prefill("qext", T=3, H=H, ctx=1024, topk=200, seed=281)
     q = wl.q.clone()
