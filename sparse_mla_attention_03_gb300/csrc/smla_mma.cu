@@ -133,24 +133,35 @@ __global__ void __launch_bounds__(NT, NST == 1 ? 4 : 2) mma_kernel(const KParams
   }
 
   // ---- gather: warp w stages tile rows 16w..16w+15 (whole rows per warp) ----
+  // Row by row: lane l copies chunk l (the 512 code bytes: one contiguous
+  // 512-byte read per warp) and lanes 0..8 copy chunk 32+l (scales and rope).
+  // A row's swizzle term ((16w + r) / 4) % 4 = (r / 4) % 4 is fixed for each
+  // unrolled r, and its row id is uniform across the warp, so an empty row
+  // costs no divergence.  swz() moves chunks 0..39 by an XOR of the term,
+  // which on byte offsets is an XOR of term * 32 (chunk 40, lane 8's second
+  // chunk, stays).
+  const uint32_t lo16 = (uint32_t)lane << 4;
+  const uint32_t hi16 = (uint32_t)(32 + lane) << 4;           // lanes 0..8: chunks 32..40
+  const uint32_t hi_xmask = lane < 8 ? 0xFFFFFFFFu : 0u;      // chunk 40 is not permuted
   auto issue = [&](int tile, int stage) -> uint32_t {
     const int slot = lo + tile * BC + warp * 16 + (lane & 15);
     int row = -1;
     if (lane < 16 && slot < hi && slot_readable<kDual>(p, slot, ts.len1))
       row = resolve_slot<kDual>(p, btr, btr2, slot, slot_index<kDual>(p, t, slot));
-    uint8_t* base = smem + L::kv + stage * BC * TS + warp * 16 * TS;
-#pragma unroll 3
-    for (int i = 0; i < 21; ++i) {
-      const int f = i * 32 + lane;
-      const int r = f / 41;
-      const int ch = f - r * 41;
-      const int rr = __shfl_sync(0xffffffffu, row, r & 15);
-      if (f < 16 * 41) {
-        const uint32_t dst = smem_u32(base + r * TS + swz(warp * 16 + r, ch) * 16);
-        if (rr >= 0)
-          cp_async16(dst, row_ptr<kDual>(p, rr) + ch * 16, 16);
-        else
-          sts_zero16(dst);
+    const uint32_t base = smem_u32(smem + L::kv + stage * BC * TS + warp * 16 * TS);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int rr = __shfl_sync(0xffffffffu, row, r);
+      const uint32_t drow = base + r * TS;
+      const uint32_t xo = (uint32_t)((r >> 2) & 3) << 5;  // swizzle term of row 16w + r, in bytes
+      const uint32_t dlo = drow + (lo16 ^ xo), dhi = drow + (hi16 ^ (xo & hi_xmask));
+      if (rr >= 0) {
+        const uint8_t* srow = row_ptr<kDual>(p, rr);
+        cp_async16(dlo, srow + lo16, 16);
+        if (lane < 9) cp_async16(dhi, srow + hi16, 16);
+      } else {
+        sts_zero16(dlo);
+        if (lane < 9) sts_zero16(dhi);
       }
     }
     return __ballot_sync(0xffffffffu, lane < 16 && row >= 0) & 0xFFFFu;
