@@ -980,6 +980,12 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
     const float sink_hi = (q4 == 0 && p.attn_sink) ? __ldg(p.attn_sink + h0 + lane + 32) : 0.f;
     load_q<kEarly>(p, smem, sbase, t, h0, c, s_qmul, s_mref, s_mneg, bars);
     const float qmul = s_qmul[0];  // the token's score factor (one q prescale for all heads)
+    // the negated reference max of every head, kept in registers: it changes
+    // only in the slow path, and reading it from shared memory on every tile
+    // put 16 broadcast loads per warp on the softmax's critical path
+    float mn[64];
+#pragma unroll
+    for (int h = 0; h < 64; ++h) mn[h] = s_mneg[h];
 
     // running sums of P per head: lane l keeps heads l and l+32 of this warp's
     // 32 candidates (summed over the warp by a transpose-reduction per tile)
@@ -1014,11 +1020,10 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       float dmax = -INFINITY;
 #pragma unroll
       for (int h4 = 0; h4 < 16; ++h4) {
-        const float4 mn = *reinterpret_cast<const float4*>(s_mneg + 4 * h4);
-        x[4 * h4 + 0] = fmaf(x[4 * h4 + 0], qmul, mn.x);
-        x[4 * h4 + 1] = fmaf(x[4 * h4 + 1], qmul, mn.y);
-        x[4 * h4 + 2] = fmaf(x[4 * h4 + 2], qmul, mn.z);
-        x[4 * h4 + 3] = fmaf(x[4 * h4 + 3], qmul, mn.w);
+        x[4 * h4 + 0] = fmaf(x[4 * h4 + 0], qmul, mn[4 * h4 + 0]);
+        x[4 * h4 + 1] = fmaf(x[4 * h4 + 1], qmul, mn[4 * h4 + 1]);
+        x[4 * h4 + 2] = fmaf(x[4 * h4 + 2], qmul, mn[4 * h4 + 2]);
+        x[4 * h4 + 3] = fmaf(x[4 * h4 + 3], qmul, mn[4 * h4 + 3]);
         dmax = fmaxf(dmax, fmaxf(fmaxf(x[4 * h4], x[4 * h4 + 1]), fmaxf(x[4 * h4 + 2], x[4 * h4 + 3])));
       }
       if (!valid) dmax = -INFINITY;
@@ -1071,12 +1076,13 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
         // scores again from TMEM, against the new references
         tmem_ld64(T_S + lane_off, x);
 #pragma unroll
+        for (int h = 0; h < 64; ++h) mn[h] = s_mneg[h];  // the references just raised
+#pragma unroll
         for (int h4 = 0; h4 < 16; ++h4) {
-          const float4 mn = *reinterpret_cast<const float4*>(s_mneg + 4 * h4);
-          x[4 * h4 + 0] = fmaf(x[4 * h4 + 0], qmul, mn.x);
-          x[4 * h4 + 1] = fmaf(x[4 * h4 + 1], qmul, mn.y);
-          x[4 * h4 + 2] = fmaf(x[4 * h4 + 2], qmul, mn.z);
-          x[4 * h4 + 3] = fmaf(x[4 * h4 + 3], qmul, mn.w);
+          x[4 * h4 + 0] = fmaf(x[4 * h4 + 0], qmul, mn[4 * h4 + 0]);
+          x[4 * h4 + 1] = fmaf(x[4 * h4 + 1], qmul, mn[4 * h4 + 1]);
+          x[4 * h4 + 2] = fmaf(x[4 * h4 + 2], qmul, mn[4 * h4 + 2]);
+          x[4 * h4 + 3] = fmaf(x[4 * h4 + 3], qmul, mn[4 * h4 + 3]);
         }
       }
       // P = exp2(x) rounded to f16 -> row c of P^T (MN-major: heads contiguous)
