@@ -1008,11 +1008,10 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       const int idx1 = idx_ahead;
       const int slot2 = slot + 2 * BM;
       idx_ahead = it + 2 < ntiles ? index_at(slot2) : -1;
+      // A failed wait (the CTA is aborting) is agreed on together with the
+      // slow-path vote below, so that a normal tile pays one barrier of the
+      // four softmax warps: the scores loaded meanwhile are then discarded.
       const bool failed = !mbar_wait(bar(B_SFULL), it & 1, s_abort, p);
-      if (bar_or(1, 128, failed)) {
-        alive = false;
-        break;
-      }
       tc_fence_after();
       float x[64];
       tmem_ld64(T_S + lane_off, x);  // one TMEM round trip per tile
@@ -1029,7 +1028,11 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
       if (!valid) dmax = -INFINITY;
       // Slow path (first tile with data, or a score 2^8 above its reference):
       // exact per-head tile maxima, raise the references, rescale sums and O^T.
-      if (bar_or(1, 128, (!refs_set && valid) || dmax > 8.f)) {
+      if (bar_or(1, 128, failed || (!refs_set && valid) || dmax > 8.f)) {
+        if (bar_or(1, 128, failed)) {
+          alive = false;
+          break;
+        }
 #pragma unroll
         for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] - s_mneg[h] : -INFINITY;  // raw scores
         s_tmax[q4 * 64 + lane] = xreduce32_at<true, 0>(x);
