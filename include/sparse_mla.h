@@ -255,8 +255,10 @@ int sparse_mla_get_error_word(smla_stream_t stream, int32_t* out_flags);
  * spun forever on mbarrier_wait_parity).  When a limit runs out, the CTA sets
  * SMLA_ERRF_TIMEOUT, stops every role, waits for its issued MMAs, frees its
  * tensor memory and returns without writing its outputs; the context stays
- * usable.  The limit in force is read when a call is made; calls already
- * queued keep theirs.
+ * usable.  A waiting thread retries with a suspend-time hint of 20 us, so a
+ * wait notices an exhausted limit (or another role's abort) within about
+ * 20 us of it.  The limit in force is read when a call is made; calls
+ * already queued keep theirs.
  */
 uint64_t sparse_mla_set_wait_limit_ns(uint64_t ns);
 
