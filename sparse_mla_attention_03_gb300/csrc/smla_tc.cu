@@ -18,7 +18,8 @@
 //          copy serves both.
 //   rope    16 KB: the rows' bf16 rope (A operand of the rope part of S^T);
 //          reused for P^T [128 cand x 64 h] f16 once S^T is done.
-//   q       72 KB: q of the token, nope f16 / rope bf16, B operand of S^T.
+//   q       72 KB: q of the token, nope f16 / rope bf16, B operand of S^T,
+//          with one power-of-two prescale for the whole token.
 //
 // Warp roles (512 threads; setmaxnreg gives 136 / 160 / 80 registers):
 //   warps 0-7   producers: warp w gathers rows 16w..16w+15 of each tile with
@@ -32,7 +33,9 @@
 //               candidate's 64 scores once, keeps a per-head reference max that
 //               is only raised when a score exceeds it by 2^8 (then O^T columns
 //               and the sums are rescaled), writes P (f16) for the PV MMA and
-//               adds P into per-head sums with warp transpose-reductions.
+//               adds P into per-head sums with warp transpose-reductions.  The
+//               token's score factor and the 64 reference maxima stay in
+//               registers, and the four warps meet at one barrier per tile.
 //   warp 12     MMA issue: S^T of a tile group by group as the producers
 //               release them, PV after the softmax; one converged warp issuing
 //               through elect.sync.
@@ -40,9 +43,9 @@
 //               tile, and half of the epilogue's stores after the last.
 //
 // Every mbarrier wait is bounded (KParams::wait_ns of global time, one second
-// unless the caller set another limit); when a limit runs out the CTA sets the
-// error word, stops, drains its issued MMAs, frees TMEM and returns without
-// writing outputs.
+// unless the caller set another limit; retries carry a 20 us suspend hint);
+// when a limit runs out the CTA sets the error word, stops, drains its issued
+// MMAs, frees TMEM and returns without writing outputs.
 #include "smla_common.cuh"
 #include "smla_launch.h"
 
