@@ -7,8 +7,10 @@
 // file's own design:
 //
 //  * One CTA = (token, head group, split).  4 warps; a tile is 64 candidate
-//    rows; warp w gathers rows 16w..16w+15 of each tile with 16-byte cp.async
-//    (coalesced: a warp copies whole 656-byte rows), two tiles in flight.
+//    rows; warp w gathers rows 16w..16w+15 of each tile with 16-byte cp.async,
+//    row by row (one contiguous 512-byte copy of the codes per row and warp,
+//    then the scales and rope).  8-head groups stage one tile per CTA and run
+//    4 CTAs per SM; 16-head groups stage two tiles.
 //  * S^T = K Q^T: warp w computes its 16 rows x all heads of the group.  The
 //    e4m3 (or int8) codes are converted to f16 in registers (one cvt per two codes, no
 //    scale); the per-128 scale multiplies the fp32 partial sum of each
