@@ -305,6 +305,26 @@ def test_q_heads_zero_subnormal_and_large(H):
     assert binding.get_error_word() == 0
 
 
+def test_q_heads_spanning_past_the_exact_range():
+    # one q prescale per token (tcgen05 kernel): a head 2^24 times the others
+    # pushes them down by about 2^-12 in f16, so their elements below about
+    # 2^-2 become f16 subnormals and lose bits; the ordinary heads must still
+    # meet the tolerances.  The large head's lse (about 1e7) is beyond what
+    # fp32 resolves to 1e-3, so only its out is compared.
+    wl = inputs.make_prefill("qspan", T=4, H=64, ctx=2048, topk=256, seed=283)
+    big = 3
+    q = wl.q.clone()
+    q[:, big] = (q[:, big].float() * 2.0 ** 24).to(torch.bfloat16)
+    wl.q = q
+    out, lse = run_prefill(wl)
+    ref_out, ref_lse = oracle_for(wl)
+    keep = [h for h in range(wl.H) if h != big]
+    assert_close(out[:, keep], lse[:, keep], ref_out[:, keep], ref_lse[:, keep], tag="q_span_2^24")
+    o = out[:, big].float().cpu().numpy().astype(np.float64)
+    assert np.abs(o - ref_out[:, big]).max() <= 2e-2
+    assert binding.get_error_word() == 0
+
+
 # ----------------------------------------------------------------------------- dual-cache form
 def run_dual(wl, decode=False, num_splits=0):
     d = to_dev(wl)
