@@ -61,7 +61,8 @@ struct KParams {
   int32_t split_len;  // slots per split, multiple of the tile width
   float* ws_o;        // [T, H, S, 512] fp32 partial outputs (normalised, sink-free)
   float* ws_lse;      // [T, H, S] fp32 partial LSE (natural log)
-  int32_t big_cache;   // 1: cache larger than a quarter of L2 (its rows mostly come from HBM)
+  int32_t big_cache;   // load policy: 0 cache within a quarter of L2, 1 larger (rows mostly
+                       // from HBM), 2 larger than L2 itself
   // Dual-cache form: a second list of slots into a second cache follows the
   // first list, whose width is padded to a multiple of 64 slots.  Unused
   // (dual 0, x_base INT32_MAX, topk2 0) for one list.

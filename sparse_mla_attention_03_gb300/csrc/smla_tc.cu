@@ -26,9 +26,12 @@
 //               coalesced 16-byte loads, converts the codes (e4m3 or int8) to
 //               f16 times the row's scale and stores them swizzled; the bf16
 //               rope is copied as is.  The next tile's rows are loaded in one
-//               burst after a tile is stored (L2-resident cache) or group by
-//               group as soon as each group is stored, with an L2 prefetch
-//               one tile further ahead (kEarly: cache beyond L2).
+//               burst after a tile is stored (kLoad 0: L2-resident cache) or
+//               group by group as soon as each group is stored, with an L2
+//               prefetch one tile further ahead (kLoad 1: cache larger than
+//               a quarter of L2; kLoad 2: larger than L2, where the rows are
+//               also read 256 bytes per row and load instruction and the
+//               128-dim groups go out in pairs).
 //   warps 8-11  softmax/epilogue: thread = TMEM lane.  Per tile it reads its
 //               candidate's 64 scores once, keeps a per-head reference max that
 //               is only raised when a score exceeds it by 2^8 (then O^T columns
@@ -427,10 +430,12 @@ __device__ __forceinline__ void xreduce64(const float (&x)[64], float& r0, float
 // coalesced (4 lanes read 64 contiguous bytes of one row), and the 16 rows'
 // scale and rope chunks (9 per row) are read as 144 consecutive (row, chunk)
 // pairs.
-template <bool kEarly, bool kDual, bool kInt8>
+template <int kLoad, bool kDual, bool kInt8>
 __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32_t sbase, uint32_t bars, int t,
                                          int len1, int lo, int hi, int ntiles, int pw, int lane,
                                          volatile int* s_abort) {
+  constexpr bool kEarly = kLoad >= 1;  // rows mostly from HBM: early per-group loads, L2 prefetch
+  constexpr bool kPairs = kLoad == 2;  // cache beyond L2: 256-byte row reads, groups in pairs
   // test hook (sparse_mla_set_test_stall): no row is gathered, so the MMA
   // issue's first wait runs out and the CTA takes its abort path
   if (p.test_stall) return;
@@ -488,6 +493,20 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
       nope[g][j] = r >= 0 ? __ldg(src + 8 * g + 4 * (j & 1) + (lane & 3)) : z;
     }
   };
+  // kPairs: pair h (0, 1) = groups 2h and 2h+1.  nope[2h + j/4][j%4] holds
+  // rows 2j (lanes 0-15) and 2j+1 (lanes 16-31), chunk 16h + l%16: each
+  // 8-lane phase of a load reads 128 contiguous bytes of one row (about 1.9
+  // cache lines, against 2.75 for two rows' 64 bytes).  Lanes 4-7 of each
+  // eight convert their upper 8 codes first, so that each 8-lane store phase
+  // covers the odd and the even 16-byte chunks of its row's two 64-dim blocks.
+  auto load_pair = [&](int h, int rowid) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = __shfl_sync(0xffffffffu, rowid, 2 * j + (lane >> 4));
+      const uint4* src = reinterpret_cast<const uint4*>(row_ptr<kDual>(p, r < 0 ? 0 : r));
+      nope[2 * h + (j >> 2)][j & 3] = r >= 0 ? __ldg(src + 16 * h + (lane & 15)) : z;
+    }
+  };
   auto load_tail = [&](int rowid) {
 #pragma unroll
     for (int k = 0; k < 5; ++k) {
@@ -500,8 +519,13 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
   };
   if (ntiles > 0) {
     const int rowid = resolve(0);
+    if constexpr (kPairs) {
+      load_pair(0, rowid);
+      load_pair(1, rowid);
+    } else {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) load_group(g, rowid);
+      for (int g = 0; g < 4; ++g) load_group(g, rowid);
+    }
     load_tail(rowid);
   }
   for (int it = 0; it < ntiles; ++it) {
@@ -523,59 +547,121 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
       }
     }
     __syncwarp();
+    if constexpr (kPairs) {
 #pragma unroll
-    for (int g = 0; g < 5; ++g) {
-      // this region of the tile is free once the previous tile's PV used it
-      // (a per-lane wait: the lanes of the converged warp poll the barrier in
-      // the same instructions and see the same phase; a warp-wide agreement on
-      // every wait cost 1% of the 16k prefill)
-      if (it > 0 && !mbar_wait(bars + 8u * (B_PV0 + (g < 4 ? g : 3)), (it - 1) & 1, s_abort, p)) return;
-      if (g < 4) {
+      for (int gp = 0; gp < 3; ++gp) {  // groups 0-1, groups 2-3, then the tail (rope)
+        // PV chunks complete in order: the pair's later chunk frees both
+        if (it > 0 && !mbar_wait(bars + 8u * (B_PV0 + (gp < 2 ? 2 * gp + 1 : 3)), (it - 1) & 1, s_abort, p))
+          return;
+        if (gp < 2) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int rl = 8 * (j >> 1) + 2 * (lane >> 3) + ((lane >> 2) & 1);
-          const int row = 16 * pw + rl;
-          const int c = 8 * g + 4 * (j & 1) + (lane & 3);  // nope chunk: dims 16c .. 16c+15
-          const __half2 sc2 = __float2half2_rn(s_sc[rl * 4 + g]);
-          const uint32_t sc2u = *reinterpret_cast<const uint32_t*>(&sc2);
-          const uint32_t w[4] = {nope[g][j].x, nope[g][j].y, nope[g][j].z, nope[g][j].w};
-          uint32_t h[8];
+          for (int j = 0; j < 8; ++j) {
+            const int rl = 2 * j + (lane >> 4);
+            const int row = 16 * pw + rl;
+            const int c = 16 * gp + (lane & 15);  // nope chunk: dims 16c .. 16c+15
+            const int odd = (lane >> 2) & 1;      // convert the upper 8 codes first
+            const uint4 nv = nope[2 * gp + (j >> 2)][j & 3];
+            const __half2 sc2 = __float2half2_rn(s_sc[rl * 4 + (c >> 3)]);
+            const uint32_t sc2u = *reinterpret_cast<const uint32_t*>(&sc2);
+            const uint32_t w[4] = {odd ? nv.z : nv.x, odd ? nv.w : nv.y, odd ? nv.x : nv.z, odd ? nv.y : nv.w};
+            uint32_t h[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if constexpr (kInt8) {
-              s8x4_to_f16x2x2(w[i], h[2 * i], h[2 * i + 1]);
-            } else {
-              asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n"
-                  " cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
-                  : "=r"(h[2 * i]), "=r"(h[2 * i + 1])
-                  : "r"(w[i]));
+            for (int i = 0; i < 4; ++i) {
+              if constexpr (kInt8) {
+                s8x4_to_f16x2x2(w[i], h[2 * i], h[2 * i + 1]);
+              } else {
+                asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n"
+                    " cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+                    : "=r"(h[2 * i]), "=r"(h[2 * i + 1])
+                    : "r"(w[i]));
+              }
+              h[2 * i] = hmul2_u32(h[2 * i], sc2u);
+              h[2 * i + 1] = hmul2_u32(h[2 * i + 1], sc2u);
             }
-            h[2 * i] = hmul2_u32(h[2 * i], sc2u);
-            h[2 * i + 1] = hmul2_u32(h[2 * i + 1], sc2u);
+            const uint32_t base = sbase + OFF_TILE + (c >> 2) * 16384;
+            const int oc = 2 * (c & 3);
+            sts128(base + sw128(row, oc + odd), make_uint4(h[0], h[1], h[2], h[3]));
+            sts128(base + sw128(row, oc + 1 - odd), make_uint4(h[4], h[5], h[6], h[7]));
           }
-          const uint32_t base = sbase + OFF_TILE + (c >> 2) * 16384;
-          const int oc = 2 * (c & 3);
-          sts128(base + sw128(row, oc), make_uint4(h[0], h[1], h[2], h[3]));
-          sts128(base + sw128(row, oc + 1), make_uint4(h[4], h[5], h[6], h[7]));
-        }
-      } else {
+        } else {
 #pragma unroll
-        for (int k = 0; k < 5; ++k) {
-          const int f = 32 * k + lane;
-          if (f < 144 && f % 9 != 0) {
-            const int rr = f / 9;
-            sts128(sbase + OFF_ROPE + sw128(16 * pw + rr, f - 9 * rr - 1), tail[k]);
+          for (int k = 0; k < 5; ++k) {
+            const int f = 32 * k + lane;
+            if (f < 144 && f % 9 != 0) {
+              const int rr = f / 9;
+              sts128(sbase + OFF_ROPE + sw128(16 * pw + rr, f - 9 * rr - 1), tail[k]);
+            }
           }
+        }
+        fence_proxy_async();
+        if (gp < 2) {
+          mbar_arrive(bars + 8u * (B_KV0 + 2 * gp));
+          mbar_arrive(bars + 8u * (B_KV0 + 2 * gp + 1));
+        } else {
+          mbar_arrive(bars + 8u * (B_KV0 + 4));
+        }
+        if (more) {  // kPairs implies kEarly
+          if (gp < 2)
+            load_pair(gp, rowid_next);
+          else
+            load_tail(rowid_next);
         }
       }
-      fence_proxy_async();
-      mbar_arrive(bars + 8u * (B_KV0 + g));
-      // the registers of this group are free: start the next tile's loads
-      if (kEarly && more) {
-        if (g < 4)
-          load_group(g, rowid_next);
-        else
-          load_tail(rowid_next);
+    } else {
+  #pragma unroll
+      for (int g = 0; g < 5; ++g) {
+        // this region of the tile is free once the previous tile's PV used it
+        // (a per-lane wait: the lanes of the converged warp poll the barrier in
+        // the same instructions and see the same phase; a warp-wide agreement on
+        // every wait cost 1% of the 16k prefill)
+        if (it > 0 && !mbar_wait(bars + 8u * (B_PV0 + (g < 4 ? g : 3)), (it - 1) & 1, s_abort, p)) return;
+        if (g < 4) {
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int rl = 8 * (j >> 1) + 2 * (lane >> 3) + ((lane >> 2) & 1);
+            const int row = 16 * pw + rl;
+            const int c = 8 * g + 4 * (j & 1) + (lane & 3);  // nope chunk: dims 16c .. 16c+15
+            const __half2 sc2 = __float2half2_rn(s_sc[rl * 4 + g]);
+            const uint32_t sc2u = *reinterpret_cast<const uint32_t*>(&sc2);
+            const uint32_t w[4] = {nope[g][j].x, nope[g][j].y, nope[g][j].z, nope[g][j].w};
+            uint32_t h[8];
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if constexpr (kInt8) {
+                s8x4_to_f16x2x2(w[i], h[2 * i], h[2 * i + 1]);
+              } else {
+                asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n"
+                    " cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+                    : "=r"(h[2 * i]), "=r"(h[2 * i + 1])
+                    : "r"(w[i]));
+              }
+              h[2 * i] = hmul2_u32(h[2 * i], sc2u);
+              h[2 * i + 1] = hmul2_u32(h[2 * i + 1], sc2u);
+            }
+            const uint32_t base = sbase + OFF_TILE + (c >> 2) * 16384;
+            const int oc = 2 * (c & 3);
+            sts128(base + sw128(row, oc), make_uint4(h[0], h[1], h[2], h[3]));
+            sts128(base + sw128(row, oc + 1), make_uint4(h[4], h[5], h[6], h[7]));
+          }
+        } else {
+  #pragma unroll
+          for (int k = 0; k < 5; ++k) {
+            const int f = 32 * k + lane;
+            if (f < 144 && f % 9 != 0) {
+              const int rr = f / 9;
+              sts128(sbase + OFF_ROPE + sw128(16 * pw + rr, f - 9 * rr - 1), tail[k]);
+            }
+          }
+        }
+        fence_proxy_async();
+        mbar_arrive(bars + 8u * (B_KV0 + g));
+        // the registers of this group are free: start the next tile's loads
+        if (kEarly && more) {
+          if (g < 4)
+            load_group(g, rowid_next);
+          else
+            load_tail(rowid_next);
+        }
       }
     }
     if (!kEarly && more) {
@@ -826,8 +912,9 @@ __device__ __forceinline__ void load_q(const KParams& p, uint8_t* smem, uint32_t
   named_bar(2, 256);                 // q, s_qmul and s_mref visible to the softmax warps and the issuer
 }
 
-template <bool kEarly, bool kDual, bool kInt8>
+template <int kLoad, bool kDual, bool kInt8>
 __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
+  constexpr bool kEarly = kLoad >= 1;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the __shared__ array so
   // that accesses through it stay shared-memory (not generic) accesses
@@ -888,7 +975,7 @@ __global__ void __launch_bounds__(NT, 1) tc_kernel(const KParams p) {
   if (warp < W_SOFT) {
     // ============================================================ producers
     asm volatile("setmaxnreg.inc.sync.aligned.u32 136;" ::: "memory");
-    producer<kEarly, kDual, kInt8>(p, smem, sbase, bars, t, ts.len1, lo, hi, ntiles, warp, lane, s_abort);
+    producer<kLoad, kDual, kInt8>(p, smem, sbase, bars, t, ts.len1, lo, hi, ntiles, warp, lane, s_abort);
   } else if (warp >= W_MMA) {
     // ============================================ q conversion, MMA issue (warp 12), epilogue
     asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
@@ -1170,15 +1257,17 @@ cudaError_t launch_tc(const KParams& p, cudaStream_t stream) {
   const int64_t grid = (int64_t)p.T * (p.H / tc_path::HG) * p.num_splits;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  // early row loads and L2 prefetch for a cache that does not stay in L2;
-  // the dual-cache form and the int8 cache format have their own instantiations
+  // load policy by cache size (p.big_cache: 0 within a quarter of L2, 1
+  // larger, 2 larger than L2); the dual-cache form and the int8 cache format
+  // have their own instantiations
   using K = void (*)(const KParams);
-  static const K kerns[8] = {
-      tc_path::tc_kernel<false, false, false>, tc_path::tc_kernel<true, false, false>,
-      tc_path::tc_kernel<false, true, false>,  tc_path::tc_kernel<true, true, false>,
-      tc_path::tc_kernel<false, false, true>,  tc_path::tc_kernel<true, false, true>,
-      tc_path::tc_kernel<false, true, true>,   tc_path::tc_kernel<true, true, true>};
-  const K kern = kerns[(p.big_cache ? 1 : 0) + (p.dual ? 2 : 0) + (p.kv_format == 1 ? 4 : 0)];
+  static const K kerns[12] = {
+      tc_path::tc_kernel<0, false, false>, tc_path::tc_kernel<1, false, false>, tc_path::tc_kernel<2, false, false>,
+      tc_path::tc_kernel<0, true, false>,  tc_path::tc_kernel<1, true, false>,  tc_path::tc_kernel<2, true, false>,
+      tc_path::tc_kernel<0, false, true>,  tc_path::tc_kernel<1, false, true>,  tc_path::tc_kernel<2, false, true>,
+      tc_path::tc_kernel<0, true, true>,   tc_path::tc_kernel<1, true, true>,   tc_path::tc_kernel<2, true, true>};
+  const int load = p.big_cache < 0 ? 0 : (p.big_cache > 2 ? 2 : p.big_cache);
+  const K kern = kerns[load + (p.dual ? 3 : 0) + (p.kv_format == 1 ? 6 : 0)];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_path::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)grid, tc_path::NT, tc_path::SMEM_BYTES, stream>>>(p);

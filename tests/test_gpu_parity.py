@@ -424,6 +424,33 @@ def test_dual_rejects_bad_extra():
                                         wl.sm_scale, extra_topk=0)
 
 
+# ----------------------------------------------------------------------------- caches beyond the whole L2
+# A cache larger than the device's L2 itself runs the tcgen05 kernel's third
+# load policy (256-byte row reads, 128-dim groups released in pairs); these
+# cover its four instantiations (e4m3 / int8, one list / two) with the full
+# oracle on every token.
+@pytest.mark.parametrize("fmt", ["e4m3", "int8"])
+@pytest.mark.parametrize("dual", [False, True])
+def test_cache_beyond_whole_l2(fmt, dual):
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    if dual:
+        wl = inputs.make_dual_decode("huge_dual", n_req=2, tokens_per_req=2, H=64, ctx_per_req=131072, topk=1024,
+                                     extra_ctx_per_req=4096, extra_topk=320, seed=353, kv_format=fmt)
+        cache = wl.kv.numel() + wl.extra_kv.numel()
+        assert cache > l2, (cache, l2)
+        out, lse = run_dual(wl, decode=True)
+        ref = oracle_dual_for(wl)
+    else:
+        wl = inputs.make_decode("huge", n_req=2, tokens_per_req=2, H=64, ctx_per_req=131072, topk=1536, seed=351,
+                                kv_format=fmt)
+        wl.topk_length = torch.tensor([1536, 700, 1, 1200], dtype=torch.int32)
+        assert wl.kv.numel() > l2, (wl.kv.numel(), l2)
+        out, lse = run_decode(wl, num_splits=0)
+        ref = oracle_for(wl)
+    assert_close(out, lse, *ref, tag=f"beyond_whole_L2_{fmt}_{'dual' if dual else 'one'}")
+    assert binding.get_error_word() == 0
+
+
 # ----------------------------------------------------------------------------- int8 cache format
 @pytest.mark.parametrize("H", [1, 8, 16, 64, 128])
 def test_int8_prefill_ragged(H):
