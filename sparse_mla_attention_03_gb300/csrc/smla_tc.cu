@@ -608,7 +608,7 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
         }
       }
     } else {
-  #pragma unroll
+#pragma unroll
       for (int g = 0; g < 5; ++g) {
         // this region of the tile is free once the previous tile's PV used it
         // (a per-lane wait: the lanes of the converged warp poll the barrier in
@@ -616,7 +616,7 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
         // every wait cost 1% of the 16k prefill)
         if (it > 0 && !mbar_wait(bars + 8u * (B_PV0 + (g < 4 ? g : 3)), (it - 1) & 1, s_abort, p)) return;
         if (g < 4) {
-  #pragma unroll
+#pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int rl = 8 * (j >> 1) + 2 * (lane >> 3) + ((lane >> 2) & 1);
             const int row = 16 * pw + rl;
@@ -625,7 +625,7 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
             const uint32_t sc2u = *reinterpret_cast<const uint32_t*>(&sc2);
             const uint32_t w[4] = {nope[g][j].x, nope[g][j].y, nope[g][j].z, nope[g][j].w};
             uint32_t h[8];
-  #pragma unroll
+#pragma unroll
             for (int i = 0; i < 4; ++i) {
               if constexpr (kInt8) {
                 s8x4_to_f16x2x2(w[i], h[2 * i], h[2 * i + 1]);
@@ -644,7 +644,7 @@ __device__ __forceinline__ void producer(const KParams& p, uint8_t* smem, uint32
             sts128(base + sw128(row, oc + 1), make_uint4(h[4], h[5], h[6], h[7]));
           }
         } else {
-  #pragma unroll
+#pragma unroll
           for (int k = 0; k < 5; ++k) {
             const int f = 32 * k + lane;
             if (f < 144 && f % 9 != 0) {
